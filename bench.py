@@ -1,0 +1,356 @@
+#!/usr/bin/env python3
+"""Throughput of the batched Muon step on one GB300 (or N independent
+replicas under torchrun), printed as one JSON line.
+
+A step is one muon_step call over the whole workload: momentum + norm, five
+Newton-Schulz iterations (Gram X X^T, Gram A A with the b/c combine, GEMM
+with the a X epilogue) and the weight update, for every matrix.  The default
+workload is one MoE layer's experts, 16 matrices of 2048 x 8192.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon NS-orthogonalised matrices/sec and TFLOP/s (5 iters) vs GB300 BF16 TC peak"
+UNIT = "matrices/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+KERNEL_SOURCES = ["muon_newton_schulz_gb300/csrc/k_tc.cu", "muon_newton_schulz_gb300/csrc/ptx_sm100.cuh",
+                  "muon_newton_schulz_gb300/csrc/muon_internal.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """dram bytes per launch of the GEMM kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kh = kernel_hash()
+    for line in open(TRAFFIC_FILE):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("kernel_hash") == kh and kv.get("workload") == workload and "gemm_bytes_per_launch" in kv:
+            return float(kv["gemm_bytes_per_launch"])
+    return None
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        try:
+            rows = [l.strip().split(", ") for l in open(self.path) if l.strip()]
+        except Exception:
+            return out
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for k, name in enumerate(names):
+                if r[5 + k].strip().lower() == "active":
+                    reasons.add(name)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                   "samples": len(sm)}
+        return out
+
+
+def oracle_baseline(workload, n_matrices: int, steps: int, warmup: int):
+    """Times the fp64 oracle on whole matrices of the workload (host cores)."""
+    import numpy as np
+    import oracle.muon_oracle as O
+    from muon_newton_schulz_gb300 import workloads as wl
+    idxs = list(range(workload.n_matrices))
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        threads = max(int(i.get("num_threads", 1)) for i in info) if info else cores
+    except Exception:
+        threads = cores
+    times = []
+    for s in range(warmup + steps):
+        i = idxs[s % len(idxs)]
+        W, G, M = wl.make_matrix(wl.spec_of(workload, i), wl.matrix_seed(workload, i), "cpu")
+        Wn, Gn, Mn = W.float().numpy(), G.numpy(), M.numpy()
+        t0 = time.perf_counter()
+        for _ in range(n_matrices):
+            O.muon_step_matrix(Wn, Gn, Mn, workload.lr, O.OracleConfig(), w_is_bf16=(W.element_size() == 2))
+        dt = time.perf_counter() - t0
+        if s >= warmup:
+            times.append(dt)
+    per_step = sum(times) / len(times)
+    return n_matrices / per_step, per_step, threads
+
+
+def run_reference(args):
+    from muon_newton_schulz_gb300 import workloads as wl
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    name = args.workload or wl.HEADLINE
+    w = wl.WORKLOADS[name]
+    rate, per_step, threads = oracle_baseline(w, 1, args.steps, args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "matrices": w.n_matrices, "shapes": sorted(set(w.shapes)),
+                   "sample_per_step": "one whole matrix of the workload, fp64 numpy oracle"},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "one whole matrix per step (the oracle on the host cores)"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args):
+    import torch
+    from muon_newton_schulz_gb300 import binding as B
+    from muon_newton_schulz_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload or wl.HEADLINE
+    w = wl.WORKLOADS[name]
+    mode = B.MUON_MODE_BF16 if args.mode == "bf16" else B.MUON_MODE_FP32_VALIDATE
+
+    B.load_library(build_if_missing=True)
+    # every rank owns whole matrices (its own replica of the workload)
+    Ws, Gs, Ms, lrs = wl.make_workload(w, dev, steady_momentum=True)
+    ms = B.MuonStep(local, mode=mode)
+    descs, n = ms.descs_from_tensors(Ws, Gs, Ms, lrs)
+    ws_bytes = ms.workspace_bytes(descs, n)
+    ws = ms.workspace(ws_bytes)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = B.muon_step(ms.h, descs, n, ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        if st != B.MUON_OK:
+            raise B.MuonError(st, B.muon_last_error_message(ms.h))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ms.check_status() != B.MUON_OK:
+        raise RuntimeError("kernel status not OK after warm-up: " + B.muon_last_error_message(ms.h))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    B.muon_set_profiling(ms.h, True)
+    B.muon_read_profile(ms.h)  # clear
+    n_launch0 = B.muon_launch_count(ms.h)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    launches = B.muon_launch_count(ms.h) - n_launch0
+    ms_total = e0.elapsed_time(e1)
+    st, prof = B.muon_read_profile(ms.h)
+    B.muon_set_profiling(ms.h, False)
+    if ms.check_status() != B.MUON_OK:
+        raise RuntimeError("kernel status not OK after the timed steps: " + B.muon_last_error_message(ms.h))
+    ms_step = ms_total / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    total_mats = w.n_matrices * world
+    value = total_mats / (ms_step / 1e3)
+    sym_flops = wl.workload_flops(w)
+    dense_flops = wl.workload_flops(w, symmetric=False)
+    peak_tf, hbm_gbs, peak_kind = peaks()
+
+    # dominant kernel: the GEMM with the a X epilogue (61% of the flops)
+    gemm_ms = prof.ms[3] / max(1, prof.launches[3])
+    gemm_flops = sum(2.0 * min(r, c) ** 2 * max(r, c) for r, c in w.shapes)
+    achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
+    traffic = measured_traffic(name)
+    phase = {B.PHASE_NAMES[i]: {"ms_per_step": prof.ms[i] / max(1, prof.steps),
+                                "launches_per_step": prof.launches[i] / max(1, prof.steps)}
+             for i in range(B.MUON_NUM_PHASES)}
+    # HBM phases against bandwidth: algorithmic bytes per element
+    elems = sum(r * c for r, c in w.shapes)
+    k1_bytes = elems * (4 + 4 + 4 + 4 + 2)       # read G, M; write M, X fp32, X bf16
+    wbytes = 2 if name != "single_256x512" else 4
+    k5_bytes = elems * (4 + 2 * wbytes)          # read X fp32; read + write W
+    phase["momentum_norm"]["gbs"] = k1_bytes / (phase["momentum_norm"]["ms_per_step"] / 1e3) / 1e9
+    phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
+
+    # end to end through the C ABI with host buffers: H2D of G, W, M, the
+    # step, D2H of W and M, every step
+    e2e = None
+    if not args.no_e2e:
+        Wh = [x.cpu().pin_memory() for x in Ws]
+        Gh = [x.cpu().pin_memory() for x in Gs]
+        Mh = [x.cpu().pin_memory() for x in Ms]
+        h2d = sum(x.numel() * x.element_size() for x in Wh + Gh + Mh)
+        d2h = sum(x.numel() * x.element_size() for x in Wh + Mh)
+        torch.cuda.synchronize(dev)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            for hsrc, d in zip(Wh + Gh + Mh, Ws + Gs + Ms):
+                d.copy_(hsrc, non_blocking=True)
+            step()
+            for d, hdst in zip(Ws + Ms, Wh + Mh):
+                hdst.copy_(d, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        dt = (time.perf_counter() - t0) / args.e2e_steps
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": total_mats / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": dt * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, per, threads = oracle_baseline(w, 1, 1, 0)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"one whole {w.shapes[0][0]}x{w.shapes[0][1]} matrix of the workload, fp64 numpy, {per:.1f} s"}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if mode == B.MUON_MODE_BF16 else "f32", "data": "synthetic",
+        "config": {"workload": name, "matrices_per_gpu": w.n_matrices, "shapes": sorted(set(w.shapes)),
+                   "ns_iters": 5, "parallelism": f"replicas x{world} (whole matrices per rank)",
+                   "l2": "inputs larger than L2: 16 x 2048x8192 fp32 G, M and the 1.5 GB of X per step"
+                   if name == wl.HEADLINE else "see workload sizes"},
+        "tflops_symmetric": sym_flops / (ms_step / 1e3) / 1e12 * world,
+        "tflops_dense_equivalent": dense_flops / (ms_step / 1e3) / 1e12 * world,
+        "frac_of_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / peak_tf,
+        "roofline": {"kernel": "k_ns_tc<GEMM> (gemm_update)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak_tf, "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": traffic,
+                     "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": gemm_ms},
+        "phases": phase,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ms.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,159 @@
+/*
+ * muon.h -- C ABI of a batched Muon optimizer step for one GB300 (sm_103a).
+ *
+ * One call of muon_step() runs, for every matrix of a ragged batch and on one
+ * CUDA stream:
+ *
+ *   1. M <- beta*M + G                       one fp32 momentum state per
+ *      parameter ("Training a 1T-Params MoE on EU public infrastructure",
+ *      tanhow.com, optimizer-state paragraph);
+ *   2. X = M (rows <= cols) or M^T (rows > cols), so that A = X X^T is the
+ *      smaller Gram matrix;  X <- X / (||X||_F + eps);
+ *   3. `ns_iters` Newton-Schulz iterations (5 per step: "ZAYA1 MoE training on
+ *      MI300X", hotelren.com/news/3048137, section 4.3), each
+ *        A  = X X^T          upper-triangle tiles only, mirrored
+ *        A2 = A A^T = A A    the same symmetric kernel reused
+ *        X <- a X + b A X + c A2 X
+ *      ("AMD GPU深度学习优化与ZAYA1大模型实践", jsqmd.com/news/1098463,
+ *      section 4.2 内存高效Muon优化器), computed as X <- a X + (b A + c A2) X;
+ *   4. W <- W - lr * scale_coeff * sqrt(max(rows, cols)) * O, O = X oriented
+ *      back to rows x cols (hotelren.com, section 4.3: lr scale
+ *      0.2 x sqrt(max(a, b))).
+ *
+ * Matrices are independent: a matrix's results do not depend on the other
+ * matrices of the batch or on their order (whole-matrix ownership as in the
+ * FlexShard paragraph of tanhow.com).
+ *
+ * Memory.  W, G, M, O_out and the workspace are device memory owned by the
+ * caller; the library never allocates or frees device memory.  A handle owns
+ * host-side state only (configuration, error text, profiling events).
+ *
+ * Streams.  muon_step() is asynchronous on `stream` (a cudaStream_t passed as
+ * void*, NULL = the legacy default stream) and never synchronises the host.
+ * W, G, M and the workspace must stay alive until the stream has passed the
+ * step.  A handle is not thread-safe; use one handle per host thread.
+ *
+ * Errors.  Every descriptor is validated before anything is launched; on an
+ * error nothing is launched and W, M are untouched.  Non-finite values in G or
+ * M are not errors: they propagate to that matrix's W and M only.
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct muon_handle_s* muon_handle;
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_ERR_INVALID_ARG = 1,   /* a NULL pointer, a bad size, stride or alignment, aliasing */
+    MUON_ERR_UNSUPPORTED = 2,   /* device is not sm_103, handle has no device, unknown mode */
+    MUON_ERR_WORKSPACE = 3,     /* workspace NULL, misaligned (256 B) or smaller than required */
+    MUON_ERR_CUDA = 4,          /* a CUDA runtime call failed; text in muon_last_error_message */
+    MUON_ERR_TIMEOUT = 5        /* a kernel gave up a bounded wait (reported by muon_check_status) */
+} muon_status;
+
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
+
+typedef enum {
+    /* bf16 tensor-core operands, fp32 accumulation, fp32 master copy of X,
+       A and (bA + cA^2) stored bf16 */
+    MUON_MODE_BF16 = 0,
+    /* fp32 operands on the CUDA cores throughout: the validation mode */
+    MUON_MODE_FP32_VALIDATE = 1
+} muon_mode;
+
+typedef struct {
+    float beta;         /* momentum factor, default 0.95 */
+    float a, b, c;      /* Newton-Schulz coefficients, default 3.4445, -4.7750, 2.0315 */
+    float eps;          /* added to ||X||_F, default 1e-7 */
+    float scale_coeff;  /* update scale coefficient, default 0.2 */
+    int32_t ns_iters;   /* Newton-Schulz iterations, 0..64, default 5 */
+    int32_t nesterov;   /* 0: NS input is the new momentum; 1: G + beta * (new momentum) */
+    int32_t mode;       /* muon_mode, default MUON_MODE_BF16 */
+} muon_config;
+
+/* One whole weight matrix, rows x cols, every buffer row-major with its own
+ * leading dimension (elements).  Pointers are device pointers, 16-byte
+ * aligned; ld * element size must be a multiple of 16 bytes; ld >= cols.
+ * W, G, M and O_out must not overlap.  rows == 0 or cols == 0 is a valid
+ * empty matrix that is skipped (its pointers may be NULL). */
+typedef struct {
+    int64_t rows, cols;
+    void* W;              /* in/out weights, dtype w_dtype */
+    int32_t w_dtype;      /* muon_dtype */
+    int32_t reserved0;
+    int64_t ldw;
+    const float* G;       /* in: fp32 gradient */
+    int64_t ldg;
+    float* M;             /* in/out: fp32 momentum */
+    int64_t ldm;
+    float lr;             /* learning rate of this matrix */
+    int32_t reserved1;
+    float* O_out;         /* optional out: fp32 O (rows x cols), or NULL */
+    int64_t ldo;
+} muon_matrix_desc;
+
+/* Per-phase device time, summed over the steps recorded since profiling was
+ * enabled or last read.  Phases: 0 momentum+norm, 1 Gram X X^T, 2 Gram A A
+ * with the b/c combine, 3 GEMM with the a X epilogue, 4 apply. */
+#define MUON_NUM_PHASES 5
+typedef struct {
+    double ms[MUON_NUM_PHASES];
+    int64_t launches[MUON_NUM_PHASES];
+    int64_t steps;
+} muon_phase_stats;
+
+/* Fills the defaults listed above. */
+void muon_config_default(muon_config* cfg);
+
+/* Creates a handle for CUDA device `device` (must be sm_103 or newer), or a
+ * host-only planning handle when device == -1 (muon_workspace_size and
+ * argument validation work; muon_step returns MUON_ERR_UNSUPPORTED after
+ * validating).  cfg NULL means defaults.  Allocates no device memory. */
+muon_status muon_create(const muon_config* cfg, int device, muon_handle* out);
+
+/* Bytes of workspace muon_step() needs for this batch (validates the
+ * descriptors; n == 0 gives 0). */
+muon_status muon_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n, size_t* bytes);
+
+/* One Muon step over `n` matrices.  `ws` is device memory of at least
+ * muon_workspace_size() bytes, 256-byte aligned, used only by this call while
+ * it runs on `stream` (its contents need not be preserved between calls).
+ * n == 0 launches nothing and returns MUON_OK. */
+muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the kernels' status word in
+ * `ws`: MUON_ERR_TIMEOUT if a kernel of an earlier step gave up a bounded
+ * wait, else MUON_OK (or MUON_ERR_CUDA if the stream reports an error). */
+muon_status muon_check_status(muon_handle h, void* ws, void* stream);
+
+muon_status muon_destroy(muon_handle h);
+
+const char* muon_status_string(muon_status s);
+
+/* Text of the last error seen by this handle ("" if none). */
+const char* muon_last_error_message(muon_handle h);
+
+/* Enables (1) or disables (0) per-phase CUDA-event timing on the launching
+ * stream.  Events are recorded around the phases of each step; at most 1024
+ * steps are kept until read. */
+muon_status muon_set_profiling(muon_handle h, int enable);
+
+/* Waits for the recorded events and returns the per-phase sums; resets them. */
+muon_status muon_read_profile(muon_handle h, muon_phase_stats* out);
+
+/* Number of kernel launches this handle has issued since it was created. */
+int64_t muon_launch_count(muon_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

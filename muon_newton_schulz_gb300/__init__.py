@@ -6,13 +6,6 @@ as hand-written sm_103a CUDA kernels behind a C ABI.
 seeded synthetic inputs.  The library is loaded on first use and its absence
 is an error, never a fallback.
 """
-from . import workloads  # noqa: F401
+from . import binding, workloads  # noqa: F401
 
-__all__ = ["workloads", "binding"]
-
-
-def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    raise AttributeError(name)
+__all__ = ["binding", "workloads"]

@@ -1,0 +1,87 @@
+"""Builds the shared library ``_build/libmuon_gb300.so`` in-tree with nvcc
+for sm_103a only.  Translation units compile in parallel; no cmake.
+
+    python -m muon_newton_schulz_gb300.build [--force]
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(BUILD, "libmuon_gb300.so")
+INCLUDE = os.path.join(ROOT, "include")
+
+CUDA_SOURCES = ["k_elementwise.cu", "k_simt_f32.cu", "k_tc.cu"]
+CXX_SOURCES = ["muon_api.cpp"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _cuda_home() -> str:
+    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH")
+    if home and os.path.isdir(home):
+        return home
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return "/usr/local/cuda"
+
+
+def _run(cmd):
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+    return r.returncode, " ".join(cmd), r.stdout
+
+
+def _stale(obj: str, deps) -> bool:
+    if not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    cuda = _cuda_home()
+    nvcc = os.path.join(cuda, "bin", "nvcc")
+    os.makedirs(BUILD, exist_ok=True)
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    headers.append(os.path.join(INCLUDE, "muon.h"))
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-I", os.path.join(cuda, "include")]
+    jobs = []
+    objs = []
+    for src in CUDA_SOURCES:
+        s = os.path.join(CSRC, src)
+        o = os.path.join(BUILD, src + ".o")
+        objs.append(o)
+        if force or _stale(o, [s] + headers):
+            jobs.append([nvcc, *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", *common, "-c", s, "-o", o])
+    for src in CXX_SOURCES:
+        s = os.path.join(CSRC, src)
+        o = os.path.join(BUILD, src + ".o")
+        objs.append(o)
+        if force or _stale(o, [s] + headers):
+            jobs.append([nvcc, "-x", "c++", "-Xcompiler", "-fPIC", *common, "-c", s, "-o", o])
+    if jobs:
+        with ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
+            results = list(ex.map(_run, jobs))
+        for rc, cmd, out in results:
+            if verbose or rc != 0:
+                sys.stderr.write(cmd + "\n" + out)
+            if rc != 0:
+                raise RuntimeError("compilation failed: " + cmd + "\n" + out)
+    if force or jobs or _stale(LIB, objs):
+        tmp = LIB + ".tmp"
+        rc, cmd, out = _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt", "-lpthread"])
+        if rc != 0:
+            raise RuntimeError("link failed: " + cmd + "\n" + out)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,304 @@
+// HBM-bound kernels of the step: momentum + sum of squares + orientation and
+// cast (K1), the per-matrix norm finish, and the scaled weight update (K5).
+//
+// All three work on 64 x 64 tiles of the caller's rows x cols matrices, one
+// 256-thread CTA per tile.  Each thread moves 4 float4 groups (16-byte,
+// coalesced along a row).  Tall matrices are transposed through a padded
+// shared-memory tile so that both the read of M and the write of X stay
+// coalesced.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "muon_internal.h"
+
+namespace muon {
+
+namespace {
+
+constexpr int kT = kEltTile;       // 64
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ int find_mat(const EltParams& p, int64_t tile) {
+  int lo = 0, hi = p.nmats - 1;
+  while (lo < hi) {  // last matrix whose tile_begin <= tile
+    int mid = (lo + hi + 1) >> 1;
+    if (p.mats[mid].tile_begin <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int64_t block_tile() {
+  return (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+}
+
+__device__ __forceinline__ double block_sum(double v, double* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  double s = 0.0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kThreads / 32; ++i) s += red[i];  // fixed order
+  }
+  return s;
+}
+
+// ---------------------------------------------------------------- K1
+// M <- beta*M + G (fp32 fma, in place); X0 = M (or G + beta*M with Nesterov)
+// written in wide orientation as fp32 master and bf16 operand; one fp64 sum
+// of squares of X0 per tile.  The normalisation 1/(||X0||+eps) is not applied
+// here: it is folded into the first iteration's epilogues.
+__global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constant__ EltParams p) {
+  __shared__ float tile[kT][kT + 1];
+  __shared__ double red[kThreads / 32];
+  const int64_t bt = block_tile();
+  if (bt >= p.total_tiles) return;
+  if (bt == 0 && threadIdx.x == 0 && p.status) *p.status = 0u;
+  const EltMat& e = p.mats[find_mat(p, bt)];
+  const int64_t lt = bt - e.tile_begin;
+  const int r0 = (int)(lt / e.tiles_c) * kT;
+  const int c0 = (int)(lt % e.tiles_c) * kT;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const float beta = p.beta;
+  float ss = 0.f;
+  double ssd = 0.0;
+
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = r0 + ty + 16 * k;
+    const int c = c0 + tx * 4;
+    float g[4] = {0.f, 0.f, 0.f, 0.f}, mm[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool row_ok = r < e.rows;
+    const bool vec = row_ok && (c + 3 < e.cols);
+    if (vec) {
+      const float4 gv = *reinterpret_cast<const float4*>(e.G + (int64_t)r * e.ldg + c);
+      const float4 mv = *reinterpret_cast<const float4*>(e.M + (int64_t)r * e.ldm + c);
+      g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
+      mm[0] = mv.x; mm[1] = mv.y; mm[2] = mv.z; mm[3] = mv.w;
+    } else if (row_ok) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c + q < e.cols) {
+          g[q] = e.G[(int64_t)r * e.ldg + c + q];
+          mm[q] = e.M[(int64_t)r * e.ldm + c + q];
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      mm[q] = fmaf(beta, mm[q], g[q]);
+      x[q] = p.nesterov ? fmaf(beta, mm[q], g[q]) : mm[q];
+      ss = fmaf(x[q], x[q], ss);
+    }
+    if (vec) {
+      *reinterpret_cast<float4*>(e.M + (int64_t)r * e.ldm + c) = make_float4(mm[0], mm[1], mm[2], mm[3]);
+    } else if (row_ok) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c + q < e.cols) e.M[(int64_t)r * e.ldm + c + q] = mm[q];
+    }
+    if (!e.tall) {
+      if (vec) {
+        *reinterpret_cast<float4*>(e.xm0 + (int64_t)r * e.ldx + c) = make_float4(x[0], x[1], x[2], x[3]);
+        if (e.xb0) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(e.xb0 + (int64_t)r * e.ldx + c) = pk;
+        }
+      } else if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < e.cols) {
+            e.xm0[(int64_t)r * e.ldx + c + q] = x[q];
+            if (e.xb0) e.xb0[(int64_t)r * e.ldx + c + q] = __float2bfloat16_rn(x[q]);
+          }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tile[ty + 16 * k][tx * 4 + q] = x[q];
+    }
+    if ((k & 1) == 1) { ssd += (double)ss; ss = 0.f; }
+  }
+
+  if (e.tall) {
+    __syncthreads();
+    // X row = caller column, X column = caller row
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int xr = c0 + ty + 16 * k;   // < cols
+      const int xc = r0 + tx * 4;        // < rows
+      if (xr >= e.cols) continue;
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = tile[tx * 4 + q][ty + 16 * k];
+      if (xc + 3 < e.rows) {
+        *reinterpret_cast<float4*>(e.xm0 + (int64_t)xr * e.ldx + xc) = make_float4(v[0], v[1], v[2], v[3]);
+        if (e.xb0) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(e.xb0 + (int64_t)xr * e.ldx + xc) = pk;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (xc + q < e.rows) {
+            e.xm0[(int64_t)xr * e.ldx + xc + q] = v[q];
+            if (e.xb0) e.xb0[(int64_t)xr * e.ldx + xc + q] = __float2bfloat16_rn(v[q]);
+          }
+      }
+    }
+  }
+
+  const double s = block_sum(ssd, red);
+  if (threadIdx.x == 0) p.partials[e.partial_begin + lt] = s;
+}
+
+// One CTA per matrix: fixed-order sum of its tile partials, then
+// scale = 1 / (sqrt(sum) + eps).
+__global__ void __launch_bounds__(kThreads) k_norm_finalize(const __grid_constant__ EltParams p) {
+  __shared__ double red[kThreads / 32];
+  const EltMat& e = p.mats[blockIdx.x];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < e.ntiles; i += kThreads) s += p.partials[e.partial_begin + i];
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) p.scale[e.mat] = (float)(1.0 / (sqrt(s) + (double)p.eps));
+}
+
+// ---------------------------------------------------------------- K5
+// W <- W - lr_eff * O, O = X_final (wide) oriented back to rows x cols.
+__global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ EltParams p) {
+  __shared__ float tile[kT][kT + 1];
+  const int64_t bt = block_tile();
+  if (bt >= p.total_tiles) return;
+  const EltMat& e = p.mats[find_mat(p, bt)];
+  const int64_t lt = bt - e.tile_begin;
+  const int r0 = (int)(lt / e.tiles_c) * kT;
+  const int c0 = (int)(lt % e.tiles_c) * kT;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const float os = p.apply_scale ? p.scale[e.mat] : 1.f;
+  const float lr = e.lr_eff;
+
+  if (e.tall) {
+    // stage X rows c0.. (caller columns), X columns r0.. (caller rows)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int xr = c0 + ty + 16 * k;
+      const int xc = r0 + tx * 4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (xr < e.cols) {
+        if (xc + 3 < e.rows) {
+          const float4 t = *reinterpret_cast<const float4*>(e.xm_final + (int64_t)xr * e.ldx + xc);
+          v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (xc + q < e.rows) v[q] = e.xm_final[(int64_t)xr * e.ldx + xc + q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tile[tx * 4 + q][ty + 16 * k] = v[q];
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = r0 + ty + 16 * k;
+    const int c = c0 + tx * 4;
+    if (r >= e.rows) continue;
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool vec = c + 3 < e.cols;
+    if (e.tall) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[q] = tile[ty + 16 * k][tx * 4 + q];
+    } else if (vec) {
+      const float4 t = *reinterpret_cast<const float4*>(e.xm_final + (int64_t)r * e.ldx + c);
+      o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c + q < e.cols) o[q] = e.xm_final[(int64_t)r * e.ldx + c + q];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] *= os;
+
+    if (e.w_bf16) {
+      __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(e.W) + (int64_t)r * e.ldw + c;
+      if (vec) {
+        uint2 pk = *reinterpret_cast<const uint2*>(W);
+        __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&pk.x);
+        __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&pk.y);
+        const float w0 = fmaf(-lr, o[0], __low2float(lo));
+        const float w1 = fmaf(-lr, o[1], __high2float(lo));
+        const float w2 = fmaf(-lr, o[2], __low2float(hi));
+        const float w3 = fmaf(-lr, o[3], __high2float(hi));
+        lo = __floats2bfloat162_rn(w0, w1);
+        hi = __floats2bfloat162_rn(w2, w3);
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(W) = pk;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < e.cols) W[q] = __float2bfloat16_rn(fmaf(-lr, o[q], __bfloat162float(W[q])));
+      }
+    } else {
+      float* W = reinterpret_cast<float*>(e.W) + (int64_t)r * e.ldw + c;
+      if (vec) {
+        float4 w = *reinterpret_cast<const float4*>(W);
+        w.x = fmaf(-lr, o[0], w.x);
+        w.y = fmaf(-lr, o[1], w.y);
+        w.z = fmaf(-lr, o[2], w.z);
+        w.w = fmaf(-lr, o[3], w.w);
+        *reinterpret_cast<float4*>(W) = w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < e.cols) W[q] = fmaf(-lr, o[q], W[q]);
+      }
+    }
+    if (e.O_out) {
+      float* Op = e.O_out + (int64_t)r * e.ldo + c;
+      if (vec) {
+        *reinterpret_cast<float4*>(Op) = make_float4(o[0], o[1], o[2], o[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < e.cols) Op[q] = o[q];
+      }
+    }
+  }
+}
+
+dim3 tile_grid(int64_t tiles) {
+  const int64_t x = tiles < 65536 ? tiles : 65536;
+  const int64_t y = (tiles + x - 1) / x;
+  return dim3((unsigned)x, (unsigned)y, 1);
+}
+
+}  // namespace
+
+int launch_momentum_norm(const EltParams& p, void* stream) {
+  if (p.total_tiles == 0) return 0;
+  k_momentum_norm<<<tile_grid(p.total_tiles), kThreads, 0, (cudaStream_t)stream>>>(p);
+  return (int)cudaGetLastError();
+}
+
+int launch_norm_finalize(const EltParams& p, void* stream) {
+  if (p.nmats == 0) return 0;
+  k_norm_finalize<<<p.nmats, kThreads, 0, (cudaStream_t)stream>>>(p);
+  return (int)cudaGetLastError();
+}
+
+int launch_apply(const EltParams& p, void* stream) {
+  if (p.total_tiles == 0) return 0;
+  k_apply<<<tile_grid(p.total_tiles), kThreads, 0, (cudaStream_t)stream>>>(p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace muon

@@ -1,0 +1,688 @@
+// C ABI of the batched Muon step: validation, batch planning (shape groups,
+// workspace layout, tile lists, TMA tensor maps) and the stream-ordered
+// launch sequence.  See include/muon.h for the contract.
+#include "muon.h"
+
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "muon_internal.h"
+
+using muon::EltMat;
+using muon::EltParams;
+using muon::PhaseGroup;
+using muon::PhaseParams;
+
+namespace {
+
+constexpr int64_t kMaxMinDim = 32768;        // m = min(rows, cols)
+constexpr int64_t kMaxMaxDim = 1ll << 24;    // n = max(rows, cols)
+constexpr int kMaxIters = 64;
+constexpr int kMaxProfiledSteps = 1024;
+
+struct StepEvents {
+  std::vector<cudaEvent_t> ev;
+  int iters = 0;
+};
+
+}  // namespace
+
+struct muon_handle_s {
+  muon_config cfg{};
+  int device = -1;
+  int sm_count = 0;
+  std::string err;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  int64_t launches = 0;
+  bool profiling = false;
+  std::vector<StepEvents> recorded;
+  std::vector<cudaEvent_t> pool;
+};
+
+namespace {
+
+struct MatPlan {
+  int desc;          // index into the caller's descriptor array
+  int64_t rows, cols, m, n;
+  bool tall;
+  int group, in_group;
+  int global;        // group.first + in_group
+  int64_t elt_tiles, tiles_c;
+  int64_t partial_begin;
+};
+
+struct GroupPlan {
+  int64_t m, n, ldx, lda;
+  int count = 0, first = 0;
+  std::vector<int> mats;  // indices into Plan::mats
+  size_t off_xm = 0, off_xb = 0, off_a = 0, off_b = 0;
+  size_t off_da = 0, off_db = 0;  // fp32 diagonal terms of A and B (tensor-core path)
+};
+
+struct Plan {
+  std::vector<MatPlan> mats;
+  std::vector<GroupPlan> groups;
+  size_t off_status = 0, off_scale = 0, off_partials = 0, bytes = 0;
+  int64_t total_partials = 0;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+muon_status fail(muon_handle h, muon_status s, const std::string& why) {
+  if (h) h->err = why;
+  return s;
+}
+
+muon_status check_config(const muon_config& c, std::string& why) {
+  if (!finite_f(c.beta) || !finite_f(c.a) || !finite_f(c.b) || !finite_f(c.c) || !finite_f(c.eps) ||
+      !finite_f(c.scale_coeff)) {
+    why = "config: beta, a, b, c, eps and scale_coeff must be finite";
+    return MUON_ERR_INVALID_ARG;
+  }
+  if (c.eps < 0.f) { why = "config: eps must be >= 0"; return MUON_ERR_INVALID_ARG; }
+  if (c.ns_iters < 0 || c.ns_iters > kMaxIters) { why = "config: ns_iters must be in [0, 64]"; return MUON_ERR_INVALID_ARG; }
+  if (c.nesterov != 0 && c.nesterov != 1) { why = "config: nesterov must be 0 or 1"; return MUON_ERR_INVALID_ARG; }
+  if (c.mode != MUON_MODE_BF16 && c.mode != MUON_MODE_FP32_VALIDATE) { why = "config: unknown mode"; return MUON_ERR_UNSUPPORTED; }
+  return MUON_OK;
+}
+
+struct Range { uintptr_t lo, hi; int desc; const char* what; };
+
+muon_status validate(const muon_matrix_desc* d, int n, std::string& why) {
+  if (n < 0) { why = "n must be >= 0"; return MUON_ERR_INVALID_ARG; }
+  if (n > 0 && !d) { why = "descs is NULL"; return MUON_ERR_INVALID_ARG; }
+  std::vector<Range> ranges;
+  for (int i = 0; i < n; ++i) {
+    const muon_matrix_desc& x = d[i];
+    const std::string at = "desc " + std::to_string(i) + ": ";
+    if (x.rows < 0 || x.cols < 0) { why = at + "rows and cols must be >= 0"; return MUON_ERR_INVALID_ARG; }
+    if (x.rows == 0 || x.cols == 0) continue;  // empty matrix: skipped
+    const int64_t m = std::min(x.rows, x.cols), nn = std::max(x.rows, x.cols);
+    if (m > kMaxMinDim || nn > kMaxMaxDim) {
+      why = at + "min(rows, cols) must be <= 32768 and max(rows, cols) <= 16777216";
+      return MUON_ERR_INVALID_ARG;
+    }
+    if (x.w_dtype != MUON_F32 && x.w_dtype != MUON_BF16) { why = at + "w_dtype must be MUON_F32 or MUON_BF16"; return MUON_ERR_INVALID_ARG; }
+    if (!x.W || !x.G || !x.M) { why = at + "W, G and M must be non-NULL"; return MUON_ERR_INVALID_ARG; }
+    const int64_t wes = x.w_dtype == MUON_BF16 ? 2 : 4;
+    struct B { const void* p; int64_t ld; int64_t es; const char* name; };
+    const B bufs[4] = {{x.W, x.ldw, wes, "W"}, {x.G, x.ldg, 4, "G"}, {x.M, x.ldm, 4, "M"}, {x.O_out, x.ldo, 4, "O_out"}};
+    for (const B& b : bufs) {
+      if (!b.p) continue;
+      if (reinterpret_cast<uintptr_t>(b.p) % 16 != 0) { why = at + b.name + " must be 16-byte aligned"; return MUON_ERR_INVALID_ARG; }
+      if (b.ld < x.cols) { why = at + "ld of " + b.name + " must be >= cols"; return MUON_ERR_INVALID_ARG; }
+      if ((b.ld * b.es) % 16 != 0) { why = at + "ld of " + b.name + " times its element size must be a multiple of 16 bytes"; return MUON_ERR_INVALID_ARG; }
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(b.p);
+      const uintptr_t hi = lo + (uintptr_t)(((x.rows - 1) * b.ld + x.cols) * b.es);
+      ranges.push_back({lo, hi, i, b.name});
+    }
+    if (!std::isfinite(x.lr)) { why = at + "lr must be finite"; return MUON_ERR_INVALID_ARG; }
+  }
+  std::sort(ranges.begin(), ranges.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < ranges.size(); ++i) {
+    if (ranges[i].lo < ranges[i - 1].hi) {
+      why = "buffers overlap: desc " + std::to_string(ranges[i - 1].desc) + " " + ranges[i - 1].what + " and desc " +
+            std::to_string(ranges[i].desc) + " " + ranges[i].what;
+      return MUON_ERR_INVALID_ARG;
+    }
+  }
+  return MUON_OK;
+}
+
+Plan build_plan(const muon_config& cfg, const muon_matrix_desc* d, int n) {
+  Plan P;
+  std::map<std::pair<int64_t, int64_t>, int> by_shape;
+  for (int i = 0; i < n; ++i) {
+    if (d[i].rows == 0 || d[i].cols == 0) continue;
+    MatPlan mp{};
+    mp.desc = i;
+    mp.rows = d[i].rows;
+    mp.cols = d[i].cols;
+    mp.tall = mp.rows > mp.cols;
+    mp.m = std::min(mp.rows, mp.cols);
+    mp.n = std::max(mp.rows, mp.cols);
+    mp.tiles_c = cdiv(mp.cols, muon::kEltTile);
+    mp.elt_tiles = cdiv(mp.rows, muon::kEltTile) * mp.tiles_c;
+    auto key = std::make_pair(mp.m, mp.n);
+    auto it = by_shape.find(key);
+    if (it == by_shape.end()) {
+      GroupPlan g;
+      g.m = mp.m;
+      g.n = mp.n;
+      g.ldx = (int64_t)align_up((size_t)mp.n, 64);
+      g.lda = (int64_t)align_up((size_t)mp.m, 64);
+      P.groups.push_back(g);
+      it = by_shape.emplace(key, (int)P.groups.size() - 1).first;
+    }
+    mp.group = it->second;
+    P.groups[mp.group].mats.push_back((int)P.mats.size());
+    P.mats.push_back(mp);
+  }
+  // largest per-tile work first (static schedules then end with short tiles)
+  std::vector<int> order(P.groups.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    const GroupPlan &x = P.groups[a], &y = P.groups[b];
+    if (x.n != y.n) return x.n > y.n;
+    return x.m > y.m;
+  });
+  std::vector<GroupPlan> sorted;
+  for (int gi : order) sorted.push_back(P.groups[gi]);
+  P.groups.swap(sorted);
+  int first = 0;
+  for (size_t g = 0; g < P.groups.size(); ++g) {
+    GroupPlan& G = P.groups[g];
+    G.first = first;
+    G.count = (int)G.mats.size();
+    for (int k = 0; k < G.count; ++k) {
+      MatPlan& mp = P.mats[G.mats[k]];
+      mp.group = (int)g;
+      mp.in_group = k;
+      mp.global = first + k;
+    }
+    first += G.count;
+  }
+  int64_t partials = 0;
+  for (MatPlan& mp : P.mats) {
+    mp.partial_begin = partials;
+    partials += mp.elt_tiles;
+  }
+  P.total_partials = partials;
+
+  const bool bf16 = cfg.mode == MUON_MODE_BF16;
+  const size_t es = bf16 ? 2 : 4;
+  size_t off = 0;
+  P.off_status = off;
+  off += 256;
+  P.off_scale = off;
+  off = align_up(off + P.mats.size() * sizeof(float), 256);
+  P.off_partials = off;
+  off = align_up(off + (size_t)partials * sizeof(double), 1024);
+  for (GroupPlan& G : P.groups) {
+    const size_t xel = (size_t)G.count * G.m * G.ldx;
+    const size_t ael = (size_t)G.count * G.m * G.lda;
+    G.off_xm = off;
+    off = align_up(off + 2 * xel * sizeof(float), 1024);
+    if (bf16) {
+      G.off_xb = off;
+      off = align_up(off + 2 * xel * 2, 1024);
+    }
+    G.off_a = off;
+    off = align_up(off + ael * es, 1024);
+    G.off_b = off;
+    off = align_up(off + ael * es, 1024);
+    if (bf16) {
+      G.off_da = off;
+      off = align_up(off + (size_t)G.count * G.lda * sizeof(float), 1024);
+      G.off_db = off;
+      off = align_up(off + (size_t)G.count * G.lda * sizeof(float), 1024);
+    }
+  }
+  P.bytes = off;
+  return P;
+}
+
+bool encode_map(muon_handle h, CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+                uint64_t ld_bytes, uint64_t mat_bytes, uint64_t buf_bytes, uint32_t box0, uint32_t box1) {
+  cuuint64_t dims[4] = {d0, d1, d2, d3};
+  cuuint64_t strides[3] = {ld_bytes, mat_bytes, buf_bytes};
+  cuuint32_t box[4] = {box0, box1, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    h->err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+// Tile counts of one group for the kernel that will run the phase.
+void set_tiles(PhaseGroup& pg, bool gram, bool tc) {
+  if (tc) {
+    pg.ni = (int32_t)cdiv(pg.m, muon::kTcM);
+    if (gram) {
+      pg.nj = (int32_t)cdiv(pg.m, muon::kTcN);
+      int t = 0;
+      for (int bj = 0; bj < pg.nj; ++bj) t += std::min(2 * bj + 2, pg.ni);
+      pg.tiles_per_mat = t;
+    } else {
+      pg.nj = (int32_t)cdiv(pg.n, muon::kTcN);
+      pg.tiles_per_mat = pg.ni * pg.nj;
+    }
+  } else {
+    pg.ni = (int32_t)cdiv(pg.m, muon::kSimtTile);
+    if (gram) {
+      pg.nj = pg.ni;
+      pg.tiles_per_mat = pg.ni * (pg.ni + 1) / 2;
+    } else {
+      pg.nj = (int32_t)cdiv(pg.n, muon::kSimtTile);
+      pg.tiles_per_mat = pg.ni * pg.nj;
+    }
+  }
+}
+
+struct DeviceGuard {
+  int old = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&old) == cudaSuccess && old != dev) changed = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(old);
+  }
+};
+
+cudaEvent_t take_event(muon_handle h) {
+  if (!h->pool.empty()) {
+    cudaEvent_t e = h->pool.back();
+    h->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+void muon_config_default(muon_config* c) {
+  if (!c) return;
+  c->beta = 0.95f;
+  c->a = 3.4445f;
+  c->b = -4.7750f;
+  c->c = 2.0315f;
+  c->eps = 1e-7f;
+  c->scale_coeff = 0.2f;
+  c->ns_iters = 5;
+  c->nesterov = 0;
+  c->mode = MUON_MODE_BF16;
+}
+
+const char* muon_status_string(muon_status s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_WORKSPACE: return "MUON_ERR_WORKSPACE";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+  }
+  return "MUON_ERR_UNKNOWN";
+}
+
+muon_status muon_create(const muon_config* cfg, int device, muon_handle* out) {
+  if (!out) return MUON_ERR_INVALID_ARG;
+  *out = nullptr;
+  muon_config c;
+  if (cfg) c = *cfg; else muon_config_default(&c);
+  std::string why;
+  muon_status st = check_config(c, why);
+  if (st != MUON_OK) return st;
+  if (device < -1) return MUON_ERR_INVALID_ARG;
+  muon_handle h = new (std::nothrow) muon_handle_s();
+  if (!h) return MUON_ERR_CUDA;
+  h->cfg = c;
+  if (device >= 0) {
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || device >= count) {
+      cudaGetLastError();
+      delete h;
+      return MUON_ERR_UNSUPPORTED;
+    }
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    // kernels are built for sm_103a, whose tcgen05 features are not forward compatible
+    if (major != 10 || minor != 3) {
+      delete h;
+      return MUON_ERR_UNSUPPORTED;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      delete h;
+      return MUON_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    h->device = device;
+    h->sm_count = sms;
+  }
+  *out = h;
+  return MUON_OK;
+}
+
+muon_status muon_destroy(muon_handle h) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  if (h->device >= 0) {
+    DeviceGuard g(h->device);
+    for (auto& s : h->recorded)
+      for (cudaEvent_t e : s.ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
+  }
+  delete h;
+  return MUON_OK;
+}
+
+const char* muon_last_error_message(muon_handle h) { return h ? h->err.c_str() : ""; }
+
+int64_t muon_launch_count(muon_handle h) { return h ? h->launches : 0; }
+
+muon_status muon_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n, size_t* bytes) {
+  if (!h || !bytes) return MUON_ERR_INVALID_ARG;
+  h->err.clear();
+  std::string why;
+  muon_status st = validate(descs, n, why);
+  if (st != MUON_OK) return fail(h, st, why);
+  Plan P = build_plan(h->cfg, descs, n);
+  *bytes = P.mats.empty() ? 0 : P.bytes;
+  return MUON_OK;
+}
+
+muon_status muon_set_profiling(muon_handle h, int enable) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
+  h->profiling = enable != 0;
+  return MUON_OK;
+}
+
+muon_status muon_read_profile(muon_handle h, muon_phase_stats* out) {
+  if (!h || !out) return MUON_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
+  DeviceGuard guard(h->device);
+  muon_status st = MUON_OK;
+  for (StepEvents& s : h->recorded) {
+    const std::vector<cudaEvent_t>& e = s.ev;
+    if (cudaEventSynchronize(e.back()) != cudaSuccess) {
+      st = fail(h, MUON_ERR_CUDA, std::string("cudaEventSynchronize: ") + cudaGetErrorString(cudaGetLastError()));
+      break;
+    }
+    float t = 0.f;
+    // e[0] start, e[1] after momentum+norm, then 3 per iteration, then after apply
+    cudaEventElapsedTime(&t, e[0], e[1]);
+    out->ms[0] += t;
+    out->launches[0] += 2;
+    for (int it = 0; it < s.iters; ++it) {
+      for (int k = 0; k < 3; ++k) {
+        cudaEventElapsedTime(&t, e[1 + 3 * it + k], e[2 + 3 * it + k]);
+        out->ms[1 + k] += t;
+        out->launches[1 + k] += 1;
+      }
+    }
+    cudaEventElapsedTime(&t, e[e.size() - 2], e[e.size() - 1]);
+    out->ms[4] += t;
+    out->launches[4] += 1;
+    out->steps += 1;
+  }
+  for (StepEvents& s : h->recorded)
+    for (cudaEvent_t e : s.ev) h->pool.push_back(e);
+  h->recorded.clear();
+  return st;
+}
+
+muon_status muon_check_status(muon_handle h, void* ws, void* stream) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
+  if (!ws) return fail(h, MUON_ERR_WORKSPACE, "workspace is NULL");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(word), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(h, MUON_ERR_CUDA, std::string("muon_check_status: ") + cudaGetErrorString(e));
+  if (word != 0) return fail(h, MUON_ERR_TIMEOUT, "a kernel gave up a bounded wait, status bits " + std::to_string(word));
+  return MUON_OK;
+}
+
+muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void* ws, size_t ws_bytes, void* stream) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  h->err.clear();
+  std::string why;
+  muon_status st = validate(descs, n, why);
+  if (st != MUON_OK) return fail(h, st, why);
+  Plan P = build_plan(h->cfg, descs, n);
+  if (P.mats.empty()) return MUON_OK;  // nothing to launch
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle: create it with a device to run steps");
+  if (!ws) return fail(h, MUON_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(h, MUON_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < P.bytes)
+    return fail(h, MUON_ERR_WORKSPACE, "workspace too small: need " + std::to_string(P.bytes) + " bytes");
+
+  DeviceGuard guard(h->device);
+  const muon_config& cfg = h->cfg;
+  const bool bf16 = cfg.mode == MUON_MODE_BF16;
+  const int iters = cfg.ns_iters;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base + P.off_status);
+  float* scale = reinterpret_cast<float*>(base + P.off_scale);
+  double* partials = reinterpret_cast<double*>(base + P.off_partials);
+
+  StepEvents se;
+  auto mark = [&]() {
+    if (!h->profiling || (int)h->recorded.size() >= kMaxProfiledSteps) return;
+    cudaEvent_t e = take_event(h);
+    if (e) {
+      cudaEventRecord(e, reinterpret_cast<cudaStream_t>(stream));
+      se.ev.push_back(e);
+    }
+  };
+  auto launched = [&](int rc, const char* what) -> muon_status {
+    if (rc != 0) {
+      return fail(h, MUON_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString((cudaError_t)rc));
+    }
+    h->launches += 1;
+    return MUON_OK;
+  };
+
+  auto xm_ptr = [&](const GroupPlan& G, int buf, int k) -> float* {
+    return reinterpret_cast<float*>(base + G.off_xm) + ((size_t)buf * G.count + k) * (size_t)G.m * G.ldx;
+  };
+  auto xb_ptr = [&](const GroupPlan& G, int buf, int k) -> __nv_bfloat16* {
+    return reinterpret_cast<__nv_bfloat16*>(base + G.off_xb) + ((size_t)buf * G.count + k) * (size_t)G.m * G.ldx;
+  };
+
+  // ---- elementwise parameter blocks (momentum/norm and apply), chunked
+  auto fill_elt = [&](EltParams& ep, size_t b, size_t e, int final_buf) {
+    std::memset(&ep, 0, sizeof(ep));
+    ep.nmats = (int32_t)(e - b);
+    ep.nesterov = cfg.nesterov;
+    ep.apply_scale = iters == 0 ? 1 : 0;
+    ep.beta = cfg.beta;
+    ep.eps = cfg.eps;
+    ep.partials = partials;
+    ep.scale = scale;
+    ep.status = b == 0 ? status : nullptr;
+    int64_t tiles = 0;
+    for (size_t i = b; i < e; ++i) {
+      const MatPlan& mp = P.mats[i];
+      const GroupPlan& G = P.groups[mp.group];
+      const muon_matrix_desc& d = descs[mp.desc];
+      EltMat& x = ep.mats[i - b];
+      x.G = d.G;
+      x.M = d.M;
+      x.W = d.W;
+      x.O_out = d.O_out;
+      x.xm0 = xm_ptr(G, 0, mp.in_group);
+      x.xb0 = bf16 ? xb_ptr(G, 0, mp.in_group) : nullptr;
+      x.xm_final = xm_ptr(G, final_buf, mp.in_group);
+      x.ldg = d.ldg;
+      x.ldm = d.ldm;
+      x.ldw = d.ldw;
+      x.ldo = d.ldo;
+      x.ldx = G.ldx;
+      x.tile_begin = tiles;
+      x.partial_begin = mp.partial_begin;
+      x.rows = (int32_t)mp.rows;
+      x.cols = (int32_t)mp.cols;
+      x.tiles_c = (int32_t)mp.tiles_c;
+      x.ntiles = (int32_t)mp.elt_tiles;
+      x.tall = mp.tall ? 1 : 0;
+      x.w_bf16 = d.w_dtype == MUON_BF16 ? 1 : 0;
+      x.mat = mp.global;
+      x.lr_eff = (float)((double)d.lr * (double)cfg.scale_coeff * std::sqrt((double)mp.n));
+      tiles += mp.elt_tiles;
+    }
+    ep.total_tiles = tiles;
+  };
+
+  EltParams* ep = new (std::nothrow) EltParams;
+  PhaseParams* pp = new (std::nothrow) PhaseParams;
+  if (!ep || !pp) {
+    delete ep;
+    delete pp;
+    return fail(h, MUON_ERR_CUDA, "host allocation failed");
+  }
+  struct Free { EltParams* a; PhaseParams* b; ~Free() { delete a; delete b; } } free_guard{ep, pp};
+
+  const int final_buf = iters % 2;
+  mark();
+  for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
+    const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
+    fill_elt(*ep, b, e, final_buf);
+    if ((st = launched(muon::launch_momentum_norm(*ep, stream), "momentum/norm kernel")) != MUON_OK) return st;
+    if ((st = launched(muon::launch_norm_finalize(*ep, stream), "norm finalize kernel")) != MUON_OK) return st;
+  }
+  mark();
+
+  // ---- Newton-Schulz iterations
+  const int grid = h->sm_count;
+  for (int it = 0; it < iters; ++it) {
+    const int cur = it % 2, nxt = 1 - cur;
+    for (int phase = 0; phase < 3; ++phase) {
+      const bool gram = phase < 2;
+      for (size_t gb = 0; gb < P.groups.size(); gb += muon::kMaxGroups) {
+        const size_t ge = std::min(P.groups.size(), gb + (size_t)muon::kMaxGroups);
+        std::memset(pp, 0, sizeof(*pp));
+        pp->ngroups = (int32_t)(ge - gb);
+        pp->status = status;
+        pp->scale = (it == 0 && phase != 1) ? scale : nullptr;
+        pp->coef_acc = phase == 1 ? cfg.c : 1.f;
+        pp->coef_prev = phase == 1 ? cfg.b : (phase == 2 ? cfg.a : 0.f);
+        int tiles = 0;
+        for (size_t gi = gb; gi < ge; ++gi) {
+          const GroupPlan& G = P.groups[gi];
+          PhaseGroup& pg = pp->g[gi - gb];
+          pg.m = (int32_t)G.m;
+          pg.n = (int32_t)G.n;
+          pg.count = G.count;
+          pg.first = G.first;
+          pg.K = (int32_t)(phase == 0 ? G.n : G.m);
+          set_tiles(pg, gram, bf16);
+          pg.tile_begin = tiles;
+          tiles += pg.tiles_per_mat * G.count;
+          pg.buf_in = phase == 1 ? 0 : cur;
+          const size_t es = bf16 ? 2 : 4;
+          uint8_t* Abuf = base + G.off_a;
+          uint8_t* Bbuf = base + G.off_b;
+          const int64_t a_stride = G.m * G.lda;
+          const int64_t x_stride = G.m * G.ldx;
+          if (bf16) {
+            // fp32 diagonal terms: the bf16 rounding residual of A's diagonal
+            // (Gram 1 -> Gram 2), and B's diagonal residual, or in the last
+            // two iterations B's exact diagonal (Gram 2 -> GEMM)
+            float* dA = reinterpret_cast<float*>(base + G.off_da);
+            float* dB = reinterpret_cast<float*>(base + G.off_db);
+            pg.diag_stride = G.lda;
+            pg.diag_in = phase == 0 ? nullptr : (phase == 1 ? dA : dB);
+            pg.diag_out = phase == 0 ? dA : (phase == 1 ? dB : nullptr);
+            pp->diag_exact = (phase == 1 && it + 2 >= iters) ? 1 : 0;
+          }
+          if (phase == 0) {          // A = s^2 X X^T
+            pg.opP = bf16 ? (const void*)xb_ptr(G, cur, 0) : (const void*)xm_ptr(G, cur, 0);
+            pg.ld_p = G.ldx;
+            pg.p_stride = x_stride;
+            pg.prev = nullptr;
+            pg.out = Abuf;
+            pg.ld_out = G.lda;
+            pg.out_stride = a_stride;
+          } else if (phase == 1) {   // B = b A + c A A^T
+            pg.opP = Abuf;
+            pg.ld_p = G.lda;
+            pg.p_stride = a_stride;
+            pg.prev = Abuf;
+            pg.ld_prev = G.lda;
+            pg.prev_stride = a_stride;
+            pg.out = Bbuf;
+            pg.ld_out = G.lda;
+            pg.out_stride = a_stride;
+          } else {                   // X' = s (a X + B X)
+            pg.opP = Bbuf;
+            pg.ld_p = G.lda;
+            pg.p_stride = a_stride;
+            pg.opX = bf16 ? (const void*)xb_ptr(G, cur, 0) : (const void*)xm_ptr(G, cur, 0);
+            pg.ld_x = G.ldx;
+            pg.x_stride = x_stride;
+            pg.prev = xm_ptr(G, cur, 0);
+            pg.ld_prev = G.ldx;
+            pg.prev_stride = x_stride;
+            pg.out = xm_ptr(G, nxt, 0);
+            pg.ld_out = G.ldx;
+            pg.out_stride = x_stride;
+            pg.out_b = (bf16 && it + 1 < iters) ? xb_ptr(G, nxt, 0) : nullptr;
+            pg.ld_outb = G.ldx;
+            pg.outb_stride = x_stride;
+          }
+          if (bf16) {
+            const uint64_t cnt = (uint64_t)G.count;
+            const uint64_t xrow = (uint64_t)G.ldx * es, xmat = (uint64_t)x_stride * es;
+            const uint64_t arow = (uint64_t)G.lda * es, amat = (uint64_t)a_stride * es;
+            bool ok = true;
+            if (phase == 0) {
+              ok = encode_map(h, &pp->map_a[gi - gb], xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 128);
+            } else if (phase == 1) {
+              ok = encode_map(h, &pp->map_a[gi - gb], Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128);
+            } else {
+              ok = encode_map(h, &pp->map_a[gi - gb], Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
+                   encode_map(h, &pp->map_b[gi - gb], xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 64);
+            }
+            if (!ok) return MUON_ERR_CUDA;
+          }
+        }
+        pp->total_tiles = tiles;
+        int rc;
+        if (bf16) rc = gram ? muon::launch_gram_tc(*pp, grid, stream) : muon::launch_gemm_tc(*pp, grid, stream);
+        else rc = gram ? muon::launch_gram_f32(*pp, stream) : muon::launch_gemm_f32(*pp, stream);
+        if ((st = launched(rc, gram ? "Gram kernel" : "GEMM kernel")) != MUON_OK) return st;
+      }
+      mark();
+    }
+  }
+
+  // ---- apply
+  for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
+    const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
+    fill_elt(*ep, b, e, final_buf);
+    if ((st = launched(muon::launch_apply(*ep, stream), "apply kernel")) != MUON_OK) return st;
+  }
+  mark();
+  if (!se.ev.empty()) {
+    se.iters = iters;
+    if ((int)se.ev.size() == 3 + 3 * iters) h->recorded.push_back(std::move(se));
+    else for (cudaEvent_t e : se.ev) h->pool.push_back(e);
+  }
+  return MUON_OK;
+}
+
+}  // extern "C"

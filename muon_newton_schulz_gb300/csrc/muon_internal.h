@@ -1,0 +1,108 @@
+// Internal structures shared by the host planner and the kernels.
+// Everything a launch needs travels in its (large, __grid_constant__) kernel
+// parameter block, so a step issues no host-to-device copies.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace muon {
+
+constexpr int kMaxGroups = 16;     // shape groups per Newton-Schulz launch
+constexpr int kMaxEltMats = 128;   // matrices per elementwise launch
+constexpr int kEltTile = 64;       // elementwise kernels work on 64 x 64 tiles
+constexpr int kSimtTile = 64;      // fp32 validation kernels: 64 x 64 output tiles
+
+// Status bits written by kernels into the workspace status word.
+constexpr uint32_t kStatusTimeoutProducer = 1u << 0;
+constexpr uint32_t kStatusTimeoutMma = 1u << 1;
+constexpr uint32_t kStatusTimeoutEpilogue = 1u << 2;
+constexpr uint32_t kStatusTimeoutDrain = 1u << 3;
+
+// One matrix as the momentum / norm / cast and apply kernels see it.
+struct EltMat {
+  const float* G;
+  float* M;
+  void* W;
+  float* O_out;
+  float* xm0;              // fp32 master copy of X0 (wide orientation), written by K1
+  __nv_bfloat16* xb0;      // bf16 operand copy of X0, or null (fp32 mode)
+  const float* xm_final;   // fp32 X after the last iteration, read by the apply kernel
+  int64_t ldg, ldm, ldw, ldo, ldx;
+  int64_t tile_begin;      // first 64x64 tile of this matrix in the launch-wide numbering
+  int64_t partial_begin;   // first partial-sum slot of this matrix
+  int32_t rows, cols;
+  int32_t tiles_c;         // 64-wide tiles along cols
+  int32_t ntiles;          // tiles of this matrix
+  int32_t tall;            // rows > cols: X is M^T
+  int32_t w_bf16;
+  int32_t mat;             // global matrix index (scale[])
+  float lr_eff;            // lr * scale_coeff * sqrt(max(rows, cols))
+};
+
+struct EltParams {
+  EltMat mats[kMaxEltMats];
+  int32_t nmats;
+  int32_t nesterov;
+  int32_t apply_scale;     // apply: multiply O by scale[] (zero iterations)
+  float beta;
+  float eps;
+  int64_t total_tiles;
+  double* partials;        // one sum of squares per 64x64 tile
+  float* scale;            // per matrix 1 / (||X0||_F + eps)
+  uint32_t* status;        // kernel status word: cleared by the first momentum CTA of a step
+};
+
+// One group of same-shape matrices (wide orientation m x n) in one
+// Newton-Schulz phase launch.
+struct PhaseGroup {
+  int32_t m, n;            // wide dims
+  int32_t count;           // matrices in the group
+  int32_t first;           // global index of its first matrix (scale[])
+  int32_t K;               // contraction length
+  int32_t ni, nj;          // output tile grid per matrix
+  int32_t tiles_per_mat;
+  int32_t tile_begin;      // first tile of this group in the launch
+  int32_t buf_in;          // ping-pong coordinate of the X operand (tensor maps)
+  // operands, for kernels that read them directly (fp32 validation path)
+  const void* opP; int64_t ld_p; int64_t p_stride;   // Gram operand / GEMM left operand
+  const void* opX; int64_t ld_x; int64_t x_stride;   // GEMM right operand
+  // epilogue
+  const void* prev; int64_t ld_prev; int64_t prev_stride;  // Gram 2: A; GEMM: X (fp32 master)
+  void* out; int64_t ld_out; int64_t out_stride;           // Gram: A or B; GEMM: X' (fp32)
+  __nv_bfloat16* out_b; int64_t ld_outb; int64_t outb_stride;  // GEMM: bf16 X' or null
+  // fp32 per-row diagonal terms (tensor-core path; null elsewhere), stride per matrix
+  const float* diag_in; float* diag_out; int64_t diag_stride;
+};
+
+struct PhaseParams {
+  CUtensorMap map_a[kMaxGroups];   // tensor-core path: left operand (and Gram right operand)
+  CUtensorMap map_b[kMaxGroups];   // tensor-core path: GEMM right operand (MN-major X)
+  PhaseGroup g[kMaxGroups];
+  int32_t ngroups;
+  int32_t total_tiles;
+  const float* scale;      // per-matrix s folded into this phase, or null
+  float coef_acc;          // Gram: multiplies the product (1 or c)
+  float coef_prev;         // Gram 2: b (times A); GEMM: a (times X)
+  int32_t diag_exact;      // Gram 2: 1 = keep B's diagonal out of the bf16 matrix (fp32 only)
+  uint32_t* status;        // kernel status word (bounded waits)
+};
+
+// Launch wrappers (defined in the .cu files).  Each returns the launch's
+// cudaError_t as int.
+int launch_momentum_norm(const EltParams& p, void* stream);
+int launch_norm_finalize(const EltParams& p, void* stream);
+int launch_apply(const EltParams& p, void* stream);
+int launch_gram_f32(const PhaseParams& p, void* stream);
+int launch_gemm_f32(const PhaseParams& p, void* stream);
+int launch_gram_tc(const PhaseParams& p, int grid, void* stream);
+int launch_gemm_tc(const PhaseParams& p, int grid, void* stream);
+int tc_smem_bytes();
+
+// Tensor-core tile shape (used by the planner to count tiles).
+constexpr int kTcM = 128;
+constexpr int kTcN = 256;
+constexpr int kTcK = 64;
+
+}  // namespace muon

@@ -31,7 +31,8 @@ float64, one library matmul per product, no blocking or fusion):
 Readings where the pages are silent (each also listed in the design notes):
   R1 coefficients (a, b, c) = (3.4445, -4.7750, 2.0315), the same every
      iteration; R2 momentum ``beta*M + G`` without dampening, beta = 0.95;
-  R3 no Nesterov; R4 eps = 1e-7 added to the norm; R5 transpose iff
+  R3 no Nesterov by default; with ``nesterov`` the NS input is
+     ``G + beta*M`` (new M), the usual Nesterov form; R4 eps = 1e-7 added to the norm; R5 transpose iff
   rows > cols; R6 no weight decay; R7 bf16 weights rounded RN-even.
 
 Pins (tests/test_oracle_pins.py): the singular-value polynomial closed form
@@ -65,6 +66,7 @@ class OracleConfig:
     eps: float = 1e-7
     scale_coeff: float = 0.2
     ns_iters: int = 5
+    nesterov: bool = False
 
 
 def momentum(M: np.ndarray, G: np.ndarray, beta: float) -> np.ndarray:
@@ -165,7 +167,10 @@ def muon_step_matrix(W: np.ndarray, G: np.ndarray, M: np.ndarray, lr: float,
     """Steps 1-6 for one matrix.  ``W`` is float32 (holding bf16 values when
     ``w_is_bf16``), ``G`` and ``M`` float32, all rows x cols."""
     M_new = momentum(M, G, cfg.beta)
-    X, transposed = orient(M_new)
+    src = M_new
+    if cfg.nesterov:
+        src = G.astype(np.float64) + float(cfg.beta) * M_new.astype(np.float64)
+    X, transposed = orient(src)
     X0 = frobenius_normalise(X, cfg.eps)
     Xk = newton_schulz(X0, cfg.a, cfg.b, cfg.c, cfg.ns_iters)
     O = Xk.T if transposed else Xk

@@ -1,0 +1,44 @@
+"""CUDA path against the fp64 oracle on seeded workloads small enough for
+the oracle, spanning several tiles and ragged edges: tolerance 2e-2 relative
+Frobenius error of O in bf16 mode and 1e-4 in the fp32 validation mode;
+momentum within one fp32 ulp; weights equal to the rounded update of the
+exported O."""
+import pytest
+
+from muon_newton_schulz_gb300 import binding as B
+from gpu_helpers import run_and_check
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["single_256x512", "experts_4x256x1024", "dense_768x768", "ragged_h384", "odd_shapes"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_fp32_validation_mode(name):
+    errs = run_and_check(name, mode=B.MUON_MODE_FP32_VALIDATE, tol_o=1e-4)
+    assert max(errs) <= 1e-4
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_bf16_mode(name):
+    errs = run_and_check(name, mode=B.MUON_MODE_BF16, tol_o=2e-2)
+    assert max(errs) <= 2e-2
+
+
+@pytest.mark.parametrize("iters", [0, 1, 2])
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_iteration_counts(iters, mode):
+    tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
+    run_and_check("odd_shapes", mode=mode, tol_o=tol, ns_iters=iters)
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_nesterov(mode):
+    tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
+    run_and_check("experts_4x256x1024", mode=mode, tol_o=tol, nesterov=True, steady_momentum=True)
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_steady_state_momentum(mode):
+    tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
+    run_and_check("ragged_h384", mode=mode, tol_o=tol, steady_momentum=True)

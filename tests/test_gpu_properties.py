@@ -1,0 +1,164 @@
+"""Properties of the CUDA path that hold at any size: bitwise determinism,
+independence from batch composition and order, multi-step momentum and
+resume, non-finite isolation, degenerate inputs, launch counts, profiling."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.muon_oracle as O
+from muon_newton_schulz_gb300 import binding as B
+from muon_newton_schulz_gb300 import workloads as wl
+from gpu_helpers import check_matrix, oracle_for, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(name, steady=False, indices=None):
+    return wl.make_workload(wl.WORKLOADS[name], "cpu", steady_momentum=steady, indices=indices)
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_bitwise_deterministic(mode):
+    Ws, Gs, Ms, lrs = _inputs("ragged_h384", steady=True)
+    a = run_gpu(Ws, Gs, Ms, lrs, mode=mode)
+    b = run_gpu(Ws, Gs, Ms, lrs, mode=mode)
+    for x, y in zip(a, b):
+        for u, v in zip(x, y):
+            assert torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u.view(torch.int32),
+                               v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32))
+
+
+def test_batch_composition_and_order_do_not_matter():
+    Ws, Gs, Ms, lrs = _inputs("ragged_h384", steady=True)
+    full = run_gpu(Ws, Gs, Ms, lrs)
+    for i in (0, 7, 10):
+        alone = run_gpu([Ws[i]], [Gs[i]], [Ms[i]], [lrs[i]])
+        assert torch.equal(alone[2][0], full[2][i])
+        assert torch.equal(alone[0][0].float(), full[0][i].float())
+    rev = list(reversed(range(len(Ws))))
+    back = run_gpu([Ws[i] for i in rev], [Gs[i] for i in rev], [Ms[i] for i in rev], [lrs[i] for i in rev])
+    for k, i in enumerate(rev):
+        assert torch.equal(back[2][k], full[2][i])
+        assert torch.equal(back[1][k], full[1][i])
+
+
+def test_multistep_and_resume():
+    Ws, Gs, Ms, lrs = _inputs("experts_4x256x1024")
+    dev = torch.device("cuda", 0)
+    Wd = [w.to(dev) for w in Ws]
+    Md = [m.to(dev) for m in Ms]
+    Od = [torch.empty(w.shape, dtype=torch.float32, device=dev) for w in Ws]
+    ms = B.MuonStep(0)
+    rng = torch.Generator().manual_seed(123)
+    saved = None
+    for step in range(3):
+        G = [torch.randn(w.shape, generator=rng) * 1e-3 for w in Ws]
+        W_before = [w.cpu() for w in Wd]
+        M_before = [m.cpu() for m in Md]
+        if step == 2:
+            saved = ([w.clone() for w in Wd], [m.clone() for m in Md], [g.clone() for g in G])
+        ms.step(Wd, [g.to(dev) for g in G], Md, lrs, Od)
+        torch.cuda.synchronize()
+        for i in range(len(Ws)):
+            res = oracle_for(W_before[i], G[i], M_before[i], lrs[i])
+            check_matrix(W_before[i], G[i], M_before[i], lrs[i], Wd[i].cpu(), Md[i].cpu(), Od[i].cpu(), res, 2e-2)
+    # resume from the checkpoint of step 2: bit-identical
+    W3 = [w.cpu() for w in Wd]
+    M3 = [m.cpu() for m in Md]
+    Wr, Mr, Gr = saved
+    ms.step(Wr, [g.to(dev) for g in Gr], Mr, lrs)
+    torch.cuda.synchronize()
+    for i in range(len(Ws)):
+        assert torch.equal(Wr[i].cpu().view(torch.int16), W3[i].view(torch.int16))
+        assert torch.equal(Mr[i].cpu(), M3[i])
+    ms.close()
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_nonfinite_stays_in_its_matrix(mode):
+    Ws, Gs, Ms, lrs = _inputs("experts_4x256x1024")
+    clean = run_gpu(Ws, Gs, Ms, lrs, mode=mode)
+    Gbad = [g.clone() for g in Gs]
+    Gbad[1][5, 7] = float("nan")
+    dirty = run_gpu(Ws, Gbad, Ms, lrs, mode=mode)
+    assert torch.isnan(dirty[1][1][5, 7])
+    assert torch.isnan(dirty[2][1]).all()
+    for i in (0, 2, 3):
+        assert torch.equal(dirty[2][i], clean[2][i])
+        assert torch.equal(dirty[0][i].float(), clean[0][i].float())
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_zero_gradient_leaves_weights(mode):
+    Ws, Gs, Ms, lrs = _inputs("odd_shapes")
+    Z = [torch.zeros_like(g) for g in Gs]
+    W, M, Oo = run_gpu(Ws, Z, [torch.zeros_like(m) for m in Ms], lrs, mode=mode)
+    for i in range(len(Ws)):
+        assert torch.count_nonzero(Oo[i]) == 0
+        assert torch.equal(W[i].float(), Ws[i].float())
+        assert torch.count_nonzero(M[i]) == 0
+
+
+def test_empty_matrices_are_skipped():
+    Ws, Gs, Ms, lrs = _inputs("odd_shapes", indices={0, 3})
+    e = torch.zeros(0, 7)
+    W, M, Oo = run_gpu([Ws[0], e.to(torch.bfloat16), Ws[1]], [Gs[0], e, Gs[1]], [Ms[0], e, Ms[1]],
+                       [lrs[0], 1.0, lrs[1]])
+    ref = run_gpu([Ws[0], Ws[1]], [Gs[0], Gs[1]], [Ms[0], Ms[1]], [lrs[0], lrs[1]])
+    assert torch.equal(Oo[0], ref[2][0]) and torch.equal(Oo[2], ref[2][1])
+
+
+def test_strided_inputs():
+    """Leading dimensions larger than cols (row padding) on every buffer."""
+    Ws, Gs, Ms, lrs = _inputs("odd_shapes", indices={0, 1})
+    dev = torch.device("cuda", 0)
+    pads = []
+    for W, G, M in zip(Ws, Gs, Ms):
+        r, c = W.shape
+        Wp = torch.zeros(r, c + 8, dtype=W.dtype, device=dev)[:, :c]
+        Gp = torch.zeros(r, c + 4, device=dev)[:, :c]
+        Mp = torch.zeros(r, c + 12, device=dev)[:, :c]
+        Wp.copy_(W)
+        Gp.copy_(G)
+        Mp.copy_(M)
+        pads.append((Wp, Gp, Mp))
+    ms = B.MuonStep(0)
+    Od = [torch.empty(w.shape, device=dev) for w in Ws]
+    ms.step([p[0] for p in pads], [p[1] for p in pads], [p[2] for p in pads], lrs, Od)
+    torch.cuda.synchronize()
+    ref = run_gpu(Ws, Gs, Ms, lrs)
+    for i in range(2):
+        assert torch.equal(Od[i].cpu(), ref[2][i])
+        assert torch.equal(pads[i][0].cpu().float(), ref[0][i].float())
+    ms.close()
+
+
+@pytest.mark.parametrize("iters", [0, 5])
+def test_launch_count_and_profile(iters):
+    Ws, Gs, Ms, lrs = _inputs("ragged_h384")
+    dev = torch.device("cuda", 0)
+    ms = B.MuonStep(0, ns_iters=iters)
+    Wd, Gd, Md = [w.to(dev) for w in Ws], [g.to(dev) for g in Gs], [m.to(dev) for m in Ms]
+    assert B.muon_set_profiling(ms.h, True) == B.MUON_OK
+    n0 = B.muon_launch_count(ms.h)
+    ms.step(Wd, Gd, Md, lrs)
+    ms.step(Wd, Gd, Md, lrs)
+    assert B.muon_launch_count(ms.h) - n0 == 2 * (2 + 3 * iters + 1)
+    st, prof = B.muon_read_profile(ms.h)
+    assert st == B.MUON_OK and prof.steps == 2
+    assert prof.launches[0] == 4 and prof.launches[4] == 2
+    if iters:
+        assert prof.launches[3] == 2 * iters and prof.ms[3] > 0
+    ms.close()
+
+
+def test_rank_deficient_gradient():
+    """A rank-3 gradient keeps rank 3 after the step (within bf16 noise)."""
+    g = torch.Generator().manual_seed(5)
+    G = (torch.randint(-4, 5, (200, 3), generator=g).float() @ torch.randint(-4, 5, (3, 520), generator=g).float())
+    W = torch.zeros(200, 520, dtype=torch.bfloat16)
+    _, _, Oo = run_gpu([W], [G], [torch.zeros_like(G)], [1e-3])
+    s = np.linalg.svd(Oo[0].double().numpy(), compute_uv=False)
+    assert s[2] > 0.1 and s[3] < 1e-2 * s[0]
+    res = oracle_for(W, G, torch.zeros_like(G), 1e-3)
+    assert np.linalg.norm(Oo[0].numpy() - res.O) / np.linalg.norm(res.O) < 2e-2

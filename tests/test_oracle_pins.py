@@ -365,3 +365,19 @@ def test_planted_missing_transpose_back_fails(monkeypatch):
     with pytest.raises(Exception):
         res = O.muon_step_matrix(np.zeros((r, c), np.float32), G, np.zeros((r, c), np.float32), 0.1)
         assert res.W.shape == (r, c) and res.O.shape == (r, c)
+
+
+def test_nesterov_from_zero_momentum_is_a_rescaling():
+    """With M = 0 the Nesterov input is (1 + beta) G, and the normalisation
+    removes any positive scale (eps = 0 makes it exact)."""
+    G = _rng(61).standard_normal((7, 12)).astype(np.float32)
+    Z = np.zeros_like(G)
+    plain = O.muon_step_matrix(Z, G, Z, 0.0, O.OracleConfig(eps=0.0))
+    nest = O.muon_step_matrix(Z, G, Z, 0.0, O.OracleConfig(eps=0.0, nesterov=True))
+    assert _rel(nest.O, plain.O) < 1e-12
+    # with a non-zero momentum the two differ
+    M = _rng(62).standard_normal((7, 12)).astype(np.float32)
+    a = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig())
+    b = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig(nesterov=True))
+    assert _rel(a.O, b.O) > 1e-3
+    assert np.array_equal(a.M, b.M)
