@@ -44,7 +44,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * TN;           // two fp32 accumulators
 constexpr int kThreads = 192;               // 6 warps
 constexpr int kEpiThreads = 128;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int EPI_BYTES = 4 * 8192;         // four epilogue warps' staging
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct Tile { int g, mat, bi, bj; };
@@ -195,25 +196,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Gram epilogue for one 32-column chunk of one row.
+// Per epilogue warp: 8 KiB of staging (all sub-buffers 1024-B aligned).
+//   Gram: row-major chunk [2] at 0 / 2048, transposed chunk [2] at 4096 / 6144
+//         (32 x 32 bf16, 64-byte rows, 64B swizzle)
+//   GEMM: X in [2] at 0 / 2048 (32 rows x 16 fp32, 64B swizzle), X' fp32 at
+//         4096 (same layout), X' bf16 at 6144 (32 rows x 16 bf16, 32B swizzle)
+constexpr int EPI_WARP_BYTES = 8192;
+
+struct EpiCtx {
+  uint8_t* buf;        // this warp's staging
+  uint64_t* xfull;     // this warp's two X-prefetch barriers (GEMM)
+  uint32_t xphase;     // parity bits of xfull[0..1]
+  int obuf;            // Gram: next staging buffer
+  int quarter, lane;
+};
+
+// Gram values of one 32-column chunk for one row (fp32, before rounding).
 //   Gram 1 (no prev):  A = alpha * acc, alpha = s^2 in the first iteration.
-//   Gram 2 (prev = A): B = b * A + c * A^2 with A = A~ + R, where A~ is the
-//     stored bf16 A and R the fp32 residual of its diagonal (diag_in), so
-//     A^2 = acc + A~ o (R_r + R_c) + R^2 on the diagonal, acc = A~ A~.
-// The diagonal goes to diag_out: its bf16 rounding residual, or with
-// diag_exact the value itself (the bf16 matrix then holds 0 there).
-__device__ __forceinline__ void gram_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, int row,
-                                           int c0, const uint32_t (&v)[32]) {
+//   Gram 2 (prev = A): B = b * A + c * A^2 with A = A~ + R, A~ the stored bf16
+//     A and R the fp32 residual of its diagonal (diag_in):
+//     A^2 = acc + A~ o (R_r + R_c) + R_r^2 on the diagonal, acc = A~ A~.
+__device__ __forceinline__ void gram_values(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, int row,
+                                            int c0, const uint32_t (&v)[32], float (&f)[32]) {
   const int m = G.m;
-  if (row >= m) return;
-  const bool full_chunk = c0 + 32 <= m;
-  float f[32];
+  const bool rv = row < m;
   if (G.prev) {
     const __nv_bfloat16* pr =
         reinterpret_cast<const __nv_bfloat16*>(G.prev) + (int64_t)tl.mat * G.prev_stride + (int64_t)row * G.ld_prev + c0;
     const float* rin = G.diag_in ? G.diag_in + (int64_t)tl.mat * G.diag_stride : nullptr;
     float pa[32], rc[32];
-    if (full_chunk) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) { pa[j] = 0.f; rc[j] = 0.f; }
+    if (rv && c0 + 32 <= m) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 u = *reinterpret_cast<const uint4*>(pr + 8 * i);
@@ -225,25 +239,25 @@ __device__ __forceinline__ void gram_chunk(const PhaseParams& p, const PhaseGrou
           pa[8 * i + 2 * h + 1] = __high2float(b2);
         }
       }
-      if (rin) {
+    } else if (rv) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < m) pa[j] = __bfloat162float(pr[j]);
+    }
+    if (rin) {
+      if (c0 + 32 <= m) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 q = *reinterpret_cast<const float4*>(rin + c0 + 4 * i);
           rc[4 * i] = q.x; rc[4 * i + 1] = q.y; rc[4 * i + 2] = q.z; rc[4 * i + 3] = q.w;
         }
-      }
-    } else {
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        pa[j] = c0 + j < m ? __bfloat162float(pr[j]) : 0.f;
-        rc[j] = (rin && c0 + j < m) ? rin[c0 + j] : 0.f;
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < m) rc[j] = rin[c0 + j];
       }
     }
-    if (!rin) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) rc[j] = 0.f;
-    }
-    const float rr = rin ? rin[row] : 0.f;
+    const float rr = (rin && rv) ? rin[row] : 0.f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       float acc = fmaf(pa[j], rr + rc[j], __uint_as_float(v[j]));
@@ -263,7 +277,16 @@ __device__ __forceinline__ void gram_chunk(const PhaseParams& p, const PhaseGrou
 #pragma unroll
     for (int j = 0; j < 32; ++j) f[j] = alpha * __uint_as_float(v[j]);
   }
-  if (G.diag_out && row >= c0 && row < c0 + 32) {
+}
+
+// Diagonal 32 x 32 block of a Gram tile: masked direct stores of r <= c and
+// the mirror of r < c; the diagonal value itself (or its bf16 residual) goes
+// to diag_out.
+__device__ __forceinline__ void gram_store_diag_block(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
+                                                      int row, int c0, float (&f)[32]) {
+  const int m = G.m;
+  if (row >= m) return;
+  if (G.diag_out) {
     float* dout = G.diag_out + (int64_t)tl.mat * G.diag_stride;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -280,105 +303,165 @@ __device__ __forceinline__ void gram_chunk(const PhaseParams& p, const PhaseGrou
   }
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(G.out) + (int64_t)tl.mat * G.out_stride;
   const int64_t ld = G.ld_out;
-  __nv_bfloat16* o = out + (int64_t)row * ld + c0;
-  if (row <= c0 && full_chunk) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 u;
-      u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
-      u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
-      u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
-      u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
-      *reinterpret_cast<uint4*>(o + 8 * i) = u;
+  for (int j = 0; j < 32; ++j) {
+    const int c = c0 + j;
+    if (c < m && row <= c) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(f[j]);
+      out[(int64_t)row * ld + c] = h;
+      if (row < c) out[(int64_t)c * ld + row] = h;
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (c0 + j < m && row <= c0 + j) o[j] = __float2bfloat16_rn(f[j]);
   }
-  // mirror the strict upper part: lanes hold consecutive rows, so each
-  // column's 32 values form one contiguous 64-byte run of row (c0 + j)
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (c0 + j < m && row < c0 + j) out[(int64_t)(c0 + j) * ld + row] = __float2bfloat16_rn(f[j]);
 }
 
-__device__ __forceinline__ void gemm_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, int row,
-                                           int c0, const uint32_t (&v)[32]) {
-  const int m = G.m, n = G.n;
-  if (row >= m) return;
-  const float s = p.scale ? p.scale[G.first + tl.mat] : 1.f;
-  // a plus this row's fp32 diagonal term of B (residual or exact diagonal)
-  const float a = p.coef_prev + (G.diag_in ? G.diag_in[(int64_t)tl.mat * G.diag_stride + row] : 0.f);
-  const float* xin = reinterpret_cast<const float*>(G.prev) + (int64_t)tl.mat * G.prev_stride +
-                     (int64_t)row * G.ld_prev + c0;
-  float* xo = reinterpret_cast<float*>(G.out) + (int64_t)tl.mat * G.out_stride + (int64_t)row * G.ld_out + c0;
-  __nv_bfloat16* xb = G.out_b ? G.out_b + (int64_t)tl.mat * G.outb_stride + (int64_t)row * G.ld_outb + c0 : nullptr;
-  float f[32];
-  if (c0 + 32 <= n) {
+// Chunk wholly above the diagonal: stage the 32 x 32 block and its transpose
+// in shared memory and write both with TMA stores.
+__device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, const Tile& tl, EpiCtx& ec, int r0,
+                                                       int c0, const float (&f)[32]) {
+  uint8_t* ro = ec.buf + ec.obuf * 2048;
+  uint8_t* tr = ec.buf + 4096 + ec.obuf * 2048;
+  const int lane = ec.lane;
+  if (lane == 0) ptx::bulk_wait_read_all();
+  __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 x = *reinterpret_cast<const float4*>(xin + 4 * i);
-      f[4 * i + 0] = s * fmaf(a, x.x, __uint_as_float(v[4 * i + 0]));
-      f[4 * i + 1] = s * fmaf(a, x.y, __uint_as_float(v[4 * i + 1]));
-      f[4 * i + 2] = s * fmaf(a, x.z, __uint_as_float(v[4 * i + 2]));
-      f[4 * i + 3] = s * fmaf(a, x.w, __uint_as_float(v[4 * i + 3]));
-      *reinterpret_cast<float4*>(xo + 4 * i) = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-    }
-    if (xb) {
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
+    u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
+    u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
+    u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
+    *reinterpret_cast<uint4*>(ro + ptx::sw64_off(lane, i)) = u;
+  }
+  // transposed block: row j (= column c0 + j), column lane (= row r0 + lane)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 u;
-        u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
-        u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
-        u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
-        u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
-        *reinterpret_cast<uint4*>(xb + 8 * i) = u;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (c0 + j < n) {
-        const float val = s * fmaf(a, xin[j], __uint_as_float(v[j]));
-        xo[j] = val;
-        if (xb) xb[j] = __float2bfloat16_rn(val);
-      }
-    }
+  for (int j = 0; j < 32; ++j)
+    *reinterpret_cast<__nv_bfloat16*>(tr + ptx::sw64_off(j, lane >> 3) + (lane & 7) * 2) = __float2bfloat16_rn(f[j]);
+  ptx::fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const CUtensorMap* mc = &p.map_c[tl.g];
+    ptx::tma_store_4d(mc, ro, c0, r0, tl.mat, 0);
+    ptx::tma_store_4d(mc, tr, r0, c0, tl.mat, 0);
+    ptx::bulk_commit();
+  }
+  ec.obuf ^= 1;
+}
+
+__device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
+                                              EpiCtx& ec, int b, int c0, int r0) {
+  if (ec.lane == 0) {
+    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2048);
+    ptx::tma_load_4d(ec.buf + b * 2048, &p.map_c[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
   }
 }
 
 template <bool kGram>
 __device__ __forceinline__ void run_epilogue(const PhaseParams& p, uint64_t* tfull, uint64_t* tempty,
-                                             uint32_t tmem_base, int quarter, int lane, volatile int* abort) {
+                                             uint32_t tmem_base, EpiCtx& ec, volatile int* abort) {
+  const int quarter = ec.quarter, lane = ec.lane;
   int acc = 0;
   uint32_t acc_phase = 0;
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+  bool ok = true;
+  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
     const Tile tl = decode_tile(p, t, kGram);
     const PhaseGroup& G = p.g[tl.g];
-    if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, abort, p.status, kStatusTimeoutEpilogue, kWaitLimitNs))
+    const int r0 = tl.bi * TM + quarter * 32;   // first row of this warp
+    const int row = r0 + lane;
+    int nch = 0;
+    if (!kGram) {
+      nch = min(TN / 16, (G.n - tl.bj * TN + 15) / 16);
+      for (int b = 0; b < 2 && b < nch; ++b) gemm_prefetch(p, G, tl, ec, b, tl.bj * TN + 16 * b, r0);
+    }
+    if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, abort, p.status, kStatusTimeoutEpilogue, kWaitLimitNs)) {
+      ok = false;
       break;
+    }
     ptx::tc_fence_after();
-    const int row0 = tl.bi * TM + quarter * 32;   // first row of this warp
-    const int row = row0 + lane;
-    const int limit = kGram ? G.m : G.n;
     const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * TN);
+    if (kGram) {
 #pragma unroll 1
-    for (int ch = 0; ch < TN / 32; ++ch) {
-      const int c0 = tl.bj * TN + ch * 32;
-      if (c0 >= limit) break;                       // uniform across the CTA
-      if (kGram && c0 + 31 < row0) continue;        // chunk wholly below the diagonal for this warp
-      uint32_t v[32];
-      ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), v);
-      ptx::tmem_ld_wait();
-      if (kGram) gram_chunk(p, G, tl, row, c0, v);
-      else gemm_chunk(p, G, tl, row, c0, v);
+      for (int ch = 0; ch < TN / 32; ++ch) {
+        const int c0 = tl.bj * TN + ch * 32;
+        if (c0 >= G.m) break;        // uniform across the CTA
+        if (c0 < r0) continue;       // wholly below the diagonal for this warp
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), v);
+        ptx::tmem_ld_wait();
+        float f[32];
+        gram_values(p, G, tl, row, c0, v, f);
+        if (c0 == r0) gram_store_diag_block(p, G, tl, row, c0, f);
+        else gram_store_upper_block(p, tl, ec, r0, c0, f);
+      }
+    } else {
+      const float s = p.scale ? p.scale[G.first + tl.mat] : 1.f;
+      // a plus this row's fp32 diagonal term of B (residual or exact diagonal)
+      const float ar = p.coef_prev +
+                       ((G.diag_in && row < G.m) ? G.diag_in[(int64_t)tl.mat * G.diag_stride + row] : 0.f);
+      uint8_t* xo = ec.buf + 4096;
+      uint8_t* xbo = ec.buf + 6144;
+#pragma unroll 1
+      for (int ch = 0; ch < nch; ++ch) {
+        const int c0 = tl.bj * TN + ch * 16;
+        const int b = ch & 1;
+        if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
+                                    kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ec.xphase ^= 1u << b;
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(ch * 16), v);
+        ptx::tmem_ld_wait();
+        const uint8_t* xi = ec.buf + b * 2048;
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 x = *reinterpret_cast<const float4*>(xi + ptx::sw64_off(lane, i));
+          f[4 * i + 0] = s * fmaf(ar, x.x, __uint_as_float(v[4 * i + 0]));
+          f[4 * i + 1] = s * fmaf(ar, x.y, __uint_as_float(v[4 * i + 1]));
+          f[4 * i + 2] = s * fmaf(ar, x.z, __uint_as_float(v[4 * i + 2]));
+          f[4 * i + 3] = s * fmaf(ar, x.w, __uint_as_float(v[4 * i + 3]));
+        }
+        ptx::fence_async_smem();
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+        if (ch + 2 < nch) gemm_prefetch(p, G, tl, ec, b, c0 + 32, r0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(xo + ptx::sw64_off(lane, i)) =
+              make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+        if (G.out_b) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            uint4 u;
+            u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
+            u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
+            u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
+            u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
+            *reinterpret_cast<uint4*>(xbo + ptx::sw32_off(lane, i)) = u;
+          }
+        }
+        ptx::fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && r0 < G.m) {  // a box that starts past the last row is not stored
+          ptx::tma_store_4d(&p.map_c[tl.g], xo, c0, r0, tl.mat, G.buf_out);
+          if (G.out_b) ptx::tma_store_4d(&p.map_d[tl.g], xbo, c0, r0, tl.mat, G.buf_out);
+          ptx::bulk_commit();
+        }
+      }
+      if (!ok) {
+        // let the X prefetches in flight land before the CTA can exit
+        for (int b = 0; b < 2; ++b) wait_drain(&ec.xfull[b], (ec.xphase >> b) & 1u);
+        break;
+      }
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(&tempty[acc]);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
+  if (lane == 0) ptx::bulk_wait_all();
+  __syncwarp();
 }
 
 template <bool kGram>
@@ -386,13 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_tc(const __grid_constant__ P
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xfull = drain + 1;                 // 2 per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -408,11 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_tc(const __grid_constant__ P
       ptx::mbar_init(&tempty[a], kEpiThreads);
     }
     ptx::mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) ptx::mbar_init(&xfull[i], 1);
     *abort = 0;
     ptx::fence_mbar_init();
     for (int g = 0; g < p.ngroups; ++g) {
       ptx::prefetch_tmap(&p.map_a[g]);
-      if (!kGram) ptx::prefetch_tmap(&p.map_b[g]);
+      ptx::prefetch_tmap(&p.map_c[g]);
+      if (!kGram) {
+        ptx::prefetch_tmap(&p.map_b[g]);
+        ptx::prefetch_tmap(&p.map_d[g]);
+      }
     }
   }
   if (warp == 1) {
@@ -431,7 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_tc(const __grid_constant__ P
     if (lane == 0) run_mma<kGram>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort);
     __syncwarp();
   } else {
-    run_epilogue<kGram>(p, tfull, tempty, tmem_base, warp & 3, lane, abort);
+    EpiCtx ec;
+    ec.buf = epi + (warp - 2) * EPI_WARP_BYTES;
+    ec.xfull = xfull + 2 * (warp - 2);
+    ec.xphase = 0;
+    ec.obuf = 0;
+    ec.quarter = warp & 3;
+    ec.lane = lane;
+    run_epilogue<kGram>(p, tfull, tempty, tmem_base, ec, abort);
   }
 
   ptx::tc_fence_before();

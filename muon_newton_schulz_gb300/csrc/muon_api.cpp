@@ -236,13 +236,14 @@ Plan build_plan(const muon_config& cfg, const muon_matrix_desc* d, int n) {
 }
 
 bool encode_map(muon_handle h, CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
-                uint64_t ld_bytes, uint64_t mat_bytes, uint64_t buf_bytes, uint32_t box0, uint32_t box1) {
+                uint64_t ld_bytes, uint64_t mat_bytes, uint64_t buf_bytes, uint32_t box0, uint32_t box1,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[4] = {d0, d1, d2, d3};
   cuuint64_t strides[3] = {ld_bytes, mat_bytes, buf_bytes};
   cuuint32_t box[4] = {box0, box1, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = h->encode(map, dtype, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     h->err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
@@ -593,6 +594,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
           pg.tile_begin = tiles;
           tiles += pg.tiles_per_mat * G.count;
           pg.buf_in = phase == 1 ? 0 : cur;
+          pg.buf_out = nxt;
           const size_t es = bf16 ? 2 : 4;
           uint8_t* Abuf = base + G.off_a;
           uint8_t* Bbuf = base + G.off_b;
@@ -649,13 +651,26 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
             const uint64_t xrow = (uint64_t)G.ldx * es, xmat = (uint64_t)x_stride * es;
             const uint64_t arow = (uint64_t)G.lda * es, amat = (uint64_t)a_stride * es;
             bool ok = true;
+            CUtensorMap* ma = &pp->map_a[gi - gb];
+            CUtensorMap* mb = &pp->map_b[gi - gb];
+            CUtensorMap* mc = &pp->map_c[gi - gb];
+            CUtensorMap* md = &pp->map_d[gi - gb];
+            const uint64_t xrow32 = (uint64_t)G.ldx * 4, xmat32 = (uint64_t)x_stride * 4;
             if (phase == 0) {
-              ok = encode_map(h, &pp->map_a[gi - gb], xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 128);
+              ok = encode_map(h, ma, xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 128) &&
+                   encode_map(h, mc, Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else if (phase == 1) {
-              ok = encode_map(h, &pp->map_a[gi - gb], Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128);
+              ok = encode_map(h, ma, Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
+                   encode_map(h, mc, Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else {
-              ok = encode_map(h, &pp->map_a[gi - gb], Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
-                   encode_map(h, &pp->map_b[gi - gb], xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 64);
+              ok = encode_map(h, ma, Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
+                   encode_map(h, mb, xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 64) &&
+                   encode_map(h, mc, xm_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow32, xmat32, xmat32 * cnt, 16, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                   encode_map(h, md, xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 16, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_32B);
             }
             if (!ok) return MUON_ERR_CUDA;
           }

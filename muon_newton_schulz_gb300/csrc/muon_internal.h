@@ -65,6 +65,7 @@ struct PhaseGroup {
   int32_t tiles_per_mat;
   int32_t tile_begin;      // first tile of this group in the launch
   int32_t buf_in;          // ping-pong coordinate of the X operand (tensor maps)
+  int32_t buf_out;         // ping-pong coordinate of the GEMM output (tensor maps)
   // operands, for kernels that read them directly (fp32 validation path)
   const void* opP; int64_t ld_p; int64_t p_stride;   // Gram operand / GEMM left operand
   const void* opX; int64_t ld_x; int64_t x_stride;   // GEMM right operand
@@ -79,6 +80,8 @@ struct PhaseGroup {
 struct PhaseParams {
   CUtensorMap map_a[kMaxGroups];   // tensor-core path: left operand (and Gram right operand)
   CUtensorMap map_b[kMaxGroups];   // tensor-core path: GEMM right operand (MN-major X)
+  CUtensorMap map_c[kMaxGroups];   // epilogue: Gram output (bf16, 32x32 box) / GEMM fp32 X in+out (16x32 box)
+  CUtensorMap map_d[kMaxGroups];   // epilogue: GEMM bf16 X out (16x32 box)
   PhaseGroup g[kMaxGroups];
   int32_t ngroups;
   int32_t total_tiles;

@@ -67,6 +67,8 @@ WORKLOADS = {
         MatrixSpec(6144, 6144, 4, "svd", log10_lo=-5.0),
         MatrixSpec(2048, 6144, 8, "svd", log10_lo=-5.0),
     ), seed_base=5000),
+    # four experts of the same shape: a profiling case that still exceeds L2
+    "experts_4x2048x8192": Workload("experts_4x2048x8192", (MatrixSpec(2048, 8192, 4, "gauss", 1e-3),), seed_base=2000),
     # scaled-down versions with the same structure, used by parity tests
     "experts_4x256x1024": Workload("experts_4x256x1024", (MatrixSpec(256, 1024, 4, "gauss", 1e-3),), seed_base=12000),
     "dense_768x768": Workload("dense_768x768", (MatrixSpec(768, 768, 1, "svd", log10_lo=-4.0),), seed_base=13000),
