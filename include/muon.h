@@ -152,6 +152,32 @@ muon_status muon_read_profile(muon_handle h, muon_phase_stats* out);
 /* Number of kernel launches this handle has issued since it was created. */
 int64_t muon_launch_count(muon_handle h);
 
+/* Size of the fixed device workspace that muon_step_noalloc uses. */
+#define MUON_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+
+/* muon_step without a caller-provided workspace, for callers that may not
+ * allocate device memory (a runtime that reserves all memory at start-up and
+ * forbids later cudaMalloc, or a plugin confined to a host framework's
+ * tensors).  The pages describe no such entry point; it exists only for
+ * those callers.
+ *
+ * The scratch space is one fixed __device__ array of
+ * MUON_STATIC_WORKSPACE_BYTES, held by every GPU that loads this library
+ * until the process exits.  The call allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.
+ *
+ * A batch whose muon_workspace_size() exceeds the array returns
+ * MUON_ERR_WORKSPACE with an explanation in muon_last_error_message and
+ * launches nothing.  All calls on a device share the array, which keeps the
+ * last call's contents (nothing in it needs to start at zero); calls that
+ * overlap on the GPU race on it and must be serialised by the caller.
+ * Otherwise identical to muon_step().  The kernels' status word sits inside
+ * the fixed array, which callers cannot address, so muon_check_status does
+ * not apply to this entry point. */
+muon_status muon_step_noalloc(muon_handle h, const muon_matrix_desc* descs, int n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -98,6 +98,8 @@ def load_library(build_if_missing: bool = False):
     lib.muon_read_profile.argtypes = [H, POINTER(muon_phase_stats)]
     lib.muon_launch_count.argtypes = [H]
     lib.muon_launch_count.restype = c_int64
+    lib.muon_step_noalloc.argtypes = [H, POINTER(muon_matrix_desc), c_int, c_void_p]
+    lib.muon_step_noalloc.restype = c_int
     for name in ("muon_create", "muon_workspace_size", "muon_step", "muon_check_status", "muon_destroy",
                  "muon_set_profiling", "muon_read_profile"):
         getattr(lib, name).restype = c_int
@@ -127,6 +129,14 @@ def muon_workspace_size(h, descs, n: int):
 
 def muon_step(h, descs, n: int, ws: int, ws_bytes: int, stream: int) -> int:
     return load_library().muon_step(h, descs, n, c_void_p(ws), ws_bytes, c_void_p(stream))
+
+
+def muon_step_noalloc(h, descs, n: int, stream: int) -> int:
+    """muon_step on the library's fixed device workspace (no allocation)."""
+    return load_library().muon_step_noalloc(h, descs, n, c_void_p(stream))
+
+
+MUON_STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 
 def muon_check_status(h, ws: int, stream: int) -> int:

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmuon_gb300.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CUDA_SOURCES = ["k_elementwise.cu", "k_simt_f32.cu", "k_tc.cu"]
+CUDA_SOURCES = ["k_elementwise.cu", "k_simt_f32.cu", "k_tc.cu", "muon_noalloc.cu"]
 CXX_SOURCES = ["muon_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

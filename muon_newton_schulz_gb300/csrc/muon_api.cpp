@@ -701,3 +701,13 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
 }
 
 }  // extern "C"
+
+namespace muon {
+
+int handle_device(::muon_handle_s* h) { return h ? h->device : -1; }
+
+void set_handle_error(::muon_handle_s* h, const std::string& msg) {
+  if (h) h->err = msg;
+}
+
+}  // namespace muon

@@ -4,8 +4,11 @@
 #pragma once
 
 #include <cstdint>
+#include <string>
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+struct muon_handle_s;
 
 namespace muon {
 
@@ -91,6 +94,10 @@ struct PhaseParams {
   int32_t diag_exact;      // Gram 2: 1 = keep B's diagonal out of the bf16 matrix (fp32 only)
   uint32_t* status;        // kernel status word (bounded waits)
 };
+
+// Handle accessors for the allocation-free entry point (defined in muon_api.cpp).
+int handle_device(::muon_handle_s* h);
+void set_handle_error(::muon_handle_s* h, const std::string& msg);
 
 // Launch wrappers (defined in the .cu files).  Each returns the launch's
 // cudaError_t as int.
