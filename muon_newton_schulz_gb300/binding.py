@@ -68,7 +68,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The in-tree library, or the file named by MUON_GB300_LIBRARY (a build
+    made with other pipeline-shape macros)."""
+    return os.environ.get("MUON_GB300_LIBRARY") or _build.LIB
 
 
 def load_library(build_if_missing: bool = False):
@@ -76,7 +78,7 @@ def load_library(build_if_missing: bool = False):
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB
+    path = library_path()
     if not os.path.exists(path):
         if not build_if_missing:
             raise RuntimeError(f"{path} is missing: run muon_newton_schulz_gb300.build.build() first")

@@ -8,17 +8,19 @@
 //       computed ("compute only the upper triangle of X X^T",
 //       jsqmd.com/news/1098463, section 4.2); each element (r, c), r <= c,
 //       is written to (r, c) and (c, r), so the result is exactly symmetric.
-//   GEMM (kGram = false): X' = s * (a X + Bm X), Bm = b A + c A^2 (m x m).
-//       The left operand is K-major (rows of Bm), the right one MN-major
-//       (rows of X), so no transposed copy of X is ever made.
+//   GEMM (kGram = false): X' = s * ((a + d) X + Bm X), Bm = b A + c A^2 (m x m)
+//       and d its fp32 per-row diagonal term.  The left operand is K-major
+//       (rows of Bm), the right one MN-major (rows of X), so no transposed
+//       copy of X is ever made.
 //
 // One CTA per SM walks a flattened list of (group, matrix, tile) entries with
 // a static stride (tile t -> CTA t mod grid): deterministic, and one launch
-// covers the whole ragged batch.  Warp 0 issues TMA loads into a 4-stage
-// shared-memory ring, warp 1 issues the MMAs (128 x 256 x 16 per instruction)
-// into one of two TMEM accumulators (2 x 256 columns), and warps 2-5 drain the
-// other accumulator through the fused epilogue, so the epilogue of tile t
-// overlaps the MMAs of tile t + 1.
+// covers the whole ragged batch.  Warp 0 issues TMA loads into a shared-memory
+// ring, warp 1 issues the MMAs (128 x 256 x 16 per instruction) into one of
+// two TMEM accumulators (2 x 256 columns), and the epilogue warps drain the
+// other accumulator, so the epilogue of tile t overlaps the MMAs of tile t + 1.
+// Epilogue data moves through swizzled shared-memory staging with TMA loads
+// (the fp32 X tile, prefetched while the MMAs run) and TMA stores.
 //
 // Every wait is bounded (one second): on a time-out the kernel records the
 // role in the status word, lets its copies and MMAs in flight finish, frees
@@ -29,6 +31,24 @@
 #include "muon_internal.h"
 #include "ptx_sm100.cuh"
 
+// Pipeline shape of each instantiation (ring stages, epilogue warps, output
+// staging buffers of the GEMM epilogue).  Defaults are the measured best.
+#ifndef MUON_GRAM_STAGES
+#define MUON_GRAM_STAGES 4
+#endif
+#ifndef MUON_GRAM_EPI_WARPS
+#define MUON_GRAM_EPI_WARPS 4
+#endif
+#ifndef MUON_GEMM_STAGES
+#define MUON_GEMM_STAGES 4
+#endif
+#ifndef MUON_GEMM_EPI_WARPS
+#define MUON_GEMM_EPI_WARPS 4
+#endif
+#ifndef MUON_GEMM_OUT_BUFS
+#define MUON_GEMM_OUT_BUFS 1
+#endif
+
 namespace muon {
 
 namespace {
@@ -37,18 +57,45 @@ constexpr int TM = kTcM;                    // 128 rows per tile (UMMA M)
 constexpr int TN = kTcN;                    // 256 columns per tile (UMMA N)
 constexpr int TK = kTcK;                    // 64 bf16 = 128 bytes = one swizzle row
 constexpr int UK = 16;                      // K per UMMA instruction
-constexpr int STAGES = 4;
 constexpr int A_BYTES = TM * TK * 2;        // 16 KiB
 constexpr int B_BYTES = TN * TK * 2;        // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * TN;           // two fp32 accumulators
-constexpr int kThreads = 192;               // 6 warps
-constexpr int kEpiThreads = 128;
-constexpr int EPI_BYTES = 4 * 8192;         // four epilogue warps' staging
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kSmemLimit = 232448;          // 227 KiB per CTA
+
+template <bool kGram>
+struct Cfg {
+  static constexpr int kStages = kGram ? MUON_GRAM_STAGES : MUON_GEMM_STAGES;
+  static constexpr int kEpiWarps = kGram ? MUON_GRAM_EPI_WARPS : MUON_GEMM_EPI_WARPS;
+  static constexpr int kOutBufs = kGram ? 2 : MUON_GEMM_OUT_BUFS;
+  static constexpr int kSlices = kEpiWarps / 4;   // epilogue warps per TMEM lane quarter
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // Gram: row-major and transposed 32x32 bf16 blocks, double-buffered (8 KiB).
+  // GEMM: two 2 KiB fp32 input buffers, then kOutBufs x (2 KiB fp32 + 1 KiB bf16).
+  static constexpr int kEpiWarpBytes = kGram ? 8192 : (kOutBufs == 1 ? 8192 : 10240);
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = 1024 + kStages * STAGE_BYTES + kEpiWarps * kEpiWarpBytes + kBarBytes;
+  static_assert(kEpiWarps % 4 == 0, "epilogue warps come in groups of four (one per TMEM lane quarter)");
+  static_assert(kOutBufs == 1 || kOutBufs == 2, "one or two output staging buffers");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory over the per-CTA limit");
+};
 
 struct Tile { int g, mat, bi, bj; };
+
+// Optional wait-time counters (build with -DMUON_TC_PROFILE): cycles summed
+// over CTAs into 64-bit slots after the status word, read from the workspace.
+//   [1] MMA waiting for a full stage   [2] MMA waiting for a free accumulator
+//   [3] TMA waiting for an empty stage [4] epilogue waiting for an accumulator
+//   [5] CTA lifetime; slots 6-10 the same for the GEMM instantiation
+#ifdef MUON_TC_PROFILE
+#define TC_PROF_T0(v) const long long v = clock64()
+#define TC_PROF_ADD(slot, v) atomicAdd(reinterpret_cast<unsigned long long*>(p.status) + (slot) + (kGram ? 0 : 5), \
+                                       (unsigned long long)(clock64() - (v)))
+#else
+#define TC_PROF_T0(v)
+#define TC_PROF_ADD(slot, v)
+#endif
 
 __device__ __forceinline__ Tile decode_tile(const PhaseParams& p, int t, bool gram) {
   int g = 0;
@@ -90,6 +137,7 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
 template <bool kGram>
 __device__ __forceinline__ void run_producer(const PhaseParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              volatile int* abort) {
+  constexpr int S = Cfg<kGram>::kStages;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t outstanding = 0, fill_parity = 0;
@@ -101,11 +149,13 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, uint8_t* smem
     const CUtensorMap* ma = &p.map_a[tl.g];
     const CUtensorMap* mb = &p.map_b[tl.g];
     for (int kb = 0; kb < nk; ++kb) {
+      TC_PROF_T0(t_e);
       if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort, p.status, kStatusTimeoutProducer,
                                   kWaitLimitNs)) {
         ok = false;
         break;
       }
+      TC_PROF_ADD(3, t_e);
       outstanding &= ~(1u << stage);
       uint8_t* sa = smem + stage * STAGE_BYTES;
       uint8_t* sb = sa + A_BYTES;
@@ -123,12 +173,12 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, uint8_t* smem
       }
       outstanding |= 1u << stage;
       fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      if (++stage == S) { stage = 0; phase ^= 1u; }
     }
   }
   if (!ok) {
     // let every copy this thread issued land before the CTA can exit
-    for (int s = 0; s < STAGES; ++s)
+    for (int s = 0; s < S; ++s)
       if ((outstanding >> s) & 1u)
         if (!wait_drain(&full[s], (fill_parity >> s) & 1u) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
   }
@@ -138,6 +188,7 @@ template <bool kGram>
 __device__ __forceinline__ void run_mma(const PhaseParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                         uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                                         volatile int* abort) {
+  constexpr int S = Cfg<kGram>::kStages;
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(TM, TN, !kGram);
   int stage = 0;
   uint32_t phase = 0;
@@ -147,17 +198,21 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, uint8_t* smem, uin
   for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
     const Tile tl = decode_tile(p, t, kGram);
     const int nk = (p.g[tl.g].K + TK - 1) / TK;
+    TC_PROF_T0(t_a);
     if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort, p.status, kStatusTimeoutMma, kWaitLimitNs)) {
       ok = false;
       break;
     }
+    TC_PROF_ADD(2, t_a);
     ptx::tc_fence_after();
     const uint32_t d = tmem_base + (uint32_t)(acc * TN);
     for (int kb = 0; kb < nk; ++kb) {
+      TC_PROF_T0(t_f);
       if (!ptx::mbar_wait_bounded(&full[stage], phase, abort, p.status, kStatusTimeoutMma, kWaitLimitNs)) {
         ok = false;
         break;
       }
+      TC_PROF_ADD(1, t_f);
       ptx::tc_fence_after();
       const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
       const uint32_t sb = sa + A_BYTES;
@@ -178,7 +233,7 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, uint8_t* smem, uin
       }
       ptx::umma_commit(&empty[stage]);
       issued = true;
-      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      if (++stage == S) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
     ptx::umma_commit(&tfull[acc]);
@@ -196,20 +251,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Per epilogue warp: 8 KiB of staging (all sub-buffers 1024-B aligned).
-//   Gram: row-major chunk [2] at 0 / 2048, transposed chunk [2] at 4096 / 6144
-//         (32 x 32 bf16, 64-byte rows, 64B swizzle)
-//   GEMM: X in [2] at 0 / 2048 (32 rows x 16 fp32, 64B swizzle), X' fp32 at
-//         4096 (same layout), X' bf16 at 6144 (32 rows x 16 bf16, 32B swizzle)
-constexpr int EPI_WARP_BYTES = 8192;
-
 struct EpiCtx {
-  uint8_t* buf;        // this warp's staging
+  uint8_t* buf;        // this warp's staging (1024-B aligned sub-buffers)
   uint64_t* xfull;     // this warp's two X-prefetch barriers (GEMM)
   uint32_t xphase;     // parity bits of xfull[0..1]
-  int obuf;            // Gram: next staging buffer
-  int quarter, lane;
+  int obuf;            // next output staging buffer
+  int quarter;         // TMEM lane quarter (warp index mod 4)
+  int slice;           // which of the kSlices column slices this warp drains
+  int lane;
 };
+
+// ---------------------------------------------------------------- Gram epilogue
 
 // Gram values of one 32-column chunk for one row (fp32, before rounding).
 //   Gram 1 (no prev):  A = alpha * acc, alpha = s^2 in the first iteration.
@@ -315,13 +367,13 @@ __device__ __forceinline__ void gram_store_diag_block(const PhaseParams& p, cons
 }
 
 // Chunk wholly above the diagonal: stage the 32 x 32 block and its transpose
-// in shared memory and write both with TMA stores.
+// in shared memory (double-buffered) and write both with TMA stores.
 __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, const Tile& tl, EpiCtx& ec, int r0,
                                                        int c0, const float (&f)[32]) {
   uint8_t* ro = ec.buf + ec.obuf * 2048;
   uint8_t* tr = ec.buf + 4096 + ec.obuf * 2048;
   const int lane = ec.lane;
-  if (lane == 0) ptx::bulk_wait_read_all();
+  if (lane == 0) ptx::bulk_wait_read_1();   // the other buffer's stores may still read
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -347,6 +399,38 @@ __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, con
   ec.obuf ^= 1;
 }
 
+__device__ __forceinline__ void gram_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
+                                                   EpiCtx& ec, uint32_t tbase, int r0) {
+  constexpr int kSl = Cfg<true>::kSlices;
+  const int row = r0 + ec.lane;
+#pragma unroll 1
+  for (int ch = ec.slice; ch < TN / 32; ch += kSl) {
+    const int c0 = tl.bj * TN + ch * 32;
+    if (c0 >= G.m) break;        // uniform across the warp
+    if (c0 < r0) continue;       // wholly below the diagonal for this warp
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), v);
+    ptx::tmem_ld_wait_regs(v);
+    float f[32];
+    gram_values(p, G, tl, row, c0, v, f);
+    if (c0 == r0) gram_store_diag_block(p, G, tl, row, c0, f);
+    else gram_store_upper_block(p, tl, ec, r0, c0, f);
+  }
+}
+
+// ---------------------------------------------------------------- GEMM epilogue
+
+// Per-warp GEMM staging: input X buffers at 0 / 2048 (32 rows x 16 fp32,
+// 64B swizzle); output buffer o holds X' fp32 at 4096 + 2048*o... laid out as
+// [fp32 x kOutBufs][bf16 x kOutBufs] (32 rows x 16 bf16, 32B swizzle).
+__device__ __forceinline__ uint8_t* gemm_xo(const EpiCtx& ec, int o) { return ec.buf + 4096 + 2048 * o; }
+__device__ __forceinline__ uint8_t* gemm_xbo(const EpiCtx& ec, int o) {
+  return ec.buf + 4096 + 2048 * Cfg<false>::kOutBufs + 1024 * o;
+}
+
+// chunk k of this warp covers columns 16 * (slice + k * kSlices) of the tile
+__device__ __forceinline__ int gemm_chunk_col(const EpiCtx& ec, int k) { return ec.slice + k * Cfg<false>::kSlices; }
+
 __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
                                               EpiCtx& ec, int b, int c0, int r0) {
   if (ec.lane == 0) {
@@ -355,145 +439,174 @@ __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseG
   }
 }
 
+// One 16-column chunk: X' = s * ((a + d) * X + acc), written as fp32 (and
+// bf16) through the staging buffers.  Returns false on a time-out.
+__device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, EpiCtx& ec,
+                                           int k, int cnt, int r0, float s, float ar, const uint32_t (&v)[16],
+                                           volatile int* abort) {
+  constexpr int kSl = Cfg<false>::kSlices;
+  const int lane = ec.lane;
+  const int b = k & 1;
+  const int c0 = tl.bj * TN + 16 * gemm_chunk_col(ec, k);
+  if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
+                              kWaitLimitNs))
+    return false;
+  ec.xphase ^= 1u << b;
+  const uint8_t* xi = ec.buf + b * 2048;
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 x = *reinterpret_cast<const float4*>(xi + ptx::sw64_off(lane, i));
+    f[4 * i + 0] = s * fmaf(ar, x.x, __uint_as_float(v[4 * i + 0]));
+    f[4 * i + 1] = s * fmaf(ar, x.y, __uint_as_float(v[4 * i + 1]));
+    f[4 * i + 2] = s * fmaf(ar, x.z, __uint_as_float(v[4 * i + 2]));
+    f[4 * i + 3] = s * fmaf(ar, x.w, __uint_as_float(v[4 * i + 3]));
+  }
+  ptx::fence_async_smem();
+  if (lane == 0) {
+    if (Cfg<false>::kOutBufs == 2) ptx::bulk_wait_read_1();
+    else ptx::bulk_wait_read_all();
+  }
+  __syncwarp();
+  if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * kSl, r0);
+  const int o = Cfg<false>::kOutBufs == 2 ? ec.obuf : 0;
+  uint8_t* xo = gemm_xo(ec, o);
+  uint8_t* xbo = gemm_xbo(ec, o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(xo + ptx::sw64_off(lane, i)) = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+  if (G.out_b) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      uint4 u;
+      u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
+      u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
+      u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
+      u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
+      *reinterpret_cast<uint4*>(xbo + ptx::sw32_off(lane, i)) = u;
+    }
+  }
+  ptx::fence_async_smem();
+  __syncwarp();
+  if (lane == 0 && r0 < G.m) {  // a box that starts past the last row is not stored
+    ptx::tma_store_4d(&p.map_c[tl.g], xo, c0, r0, tl.mat, G.buf_out);
+    if (G.out_b) ptx::tma_store_4d(&p.map_d[tl.g], xbo, c0, r0, tl.mat, G.buf_out);
+  }
+  if (lane == 0) ptx::bulk_commit();   // one group per chunk (possibly empty)
+  ec.obuf ^= 1;
+  return true;
+}
+
+// The GEMM tile's epilogue for this warp; TMEM loads of chunk k + 1 are in
+// flight while chunk k is processed.
+__device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
+                                                   EpiCtx& ec, uint32_t tbase, int r0, int cnt, volatile int* abort) {
+  const int row = r0 + ec.lane;
+  const float s = p.scale ? p.scale[G.first + tl.mat] : 1.f;
+  // a plus this row's fp32 diagonal term of B (residual or exact diagonal)
+  const float ar = p.coef_prev + ((G.diag_in && row < G.m) ? G.diag_in[(int64_t)tl.mat * G.diag_stride + row] : 0.f);
+  if (cnt <= 0) return true;
+  uint32_t va[16], vb[16];
+  ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, 0)), va);
+  ptx::tmem_ld_wait_regs(va);
+#pragma unroll 1
+  for (int k = 0; k < cnt; k += 2) {
+    const bool has1 = k + 1 < cnt;
+    if (has1) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, k + 1)), vb);
+    if (!gemm_chunk(p, G, tl, ec, k, cnt, r0, s, ar, va, abort)) {
+      if (has1) ptx::tmem_ld_wait_regs(vb);
+      return false;
+    }
+    if (has1) {
+      ptx::tmem_ld_wait_regs(vb);
+      const bool has2 = k + 2 < cnt;
+      if (has2) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, k + 2)), va);
+      const bool okb = gemm_chunk(p, G, tl, ec, k + 1, cnt, r0, s, ar, vb, abort);
+      if (has2) ptx::tmem_ld_wait_regs(va);
+      if (!okb) return false;
+    }
+  }
+  return true;
+}
+
 template <bool kGram>
 __device__ __forceinline__ void run_epilogue(const PhaseParams& p, uint64_t* tfull, uint64_t* tempty,
                                              uint32_t tmem_base, EpiCtx& ec, volatile int* abort) {
-  const int quarter = ec.quarter, lane = ec.lane;
+  constexpr int kSl = Cfg<kGram>::kSlices;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true;
   for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
     const Tile tl = decode_tile(p, t, kGram);
     const PhaseGroup& G = p.g[tl.g];
-    const int r0 = tl.bi * TM + quarter * 32;   // first row of this warp
-    const int row = r0 + lane;
-    int nch = 0;
+    const int r0 = tl.bi * TM + ec.quarter * 32;   // first row of this warp
+    int cnt = 0;
     if (!kGram) {
-      nch = min(TN / 16, (G.n - tl.bj * TN + 15) / 16);
-      for (int b = 0; b < 2 && b < nch; ++b) gemm_prefetch(p, G, tl, ec, b, tl.bj * TN + 16 * b, r0);
+      const int nch = min(TN / 16, (G.n - tl.bj * TN + 15) / 16);
+      cnt = nch > ec.slice ? (nch - ec.slice + kSl - 1) / kSl : 0;
+      for (int k = 0; k < 2 && k < cnt; ++k) gemm_prefetch(p, G, tl, ec, k, tl.bj * TN + 16 * gemm_chunk_col(ec, k), r0);
     }
+    TC_PROF_T0(t_t);
     if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, abort, p.status, kStatusTimeoutEpilogue, kWaitLimitNs)) {
       ok = false;
-      break;
     }
-    ptx::tc_fence_after();
-    const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * TN);
-    if (kGram) {
-#pragma unroll 1
-      for (int ch = 0; ch < TN / 32; ++ch) {
-        const int c0 = tl.bj * TN + ch * 32;
-        if (c0 >= G.m) break;        // uniform across the CTA
-        if (c0 < r0) continue;       // wholly below the diagonal for this warp
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), v);
-        ptx::tmem_ld_wait();
-        float f[32];
-        gram_values(p, G, tl, row, c0, v, f);
-        if (c0 == r0) gram_store_diag_block(p, G, tl, row, c0, f);
-        else gram_store_upper_block(p, tl, ec, r0, c0, f);
-      }
-    } else {
-      const float s = p.scale ? p.scale[G.first + tl.mat] : 1.f;
-      // a plus this row's fp32 diagonal term of B (residual or exact diagonal)
-      const float ar = p.coef_prev +
-                       ((G.diag_in && row < G.m) ? G.diag_in[(int64_t)tl.mat * G.diag_stride + row] : 0.f);
-      uint8_t* xo = ec.buf + 4096;
-      uint8_t* xbo = ec.buf + 6144;
-#pragma unroll 1
-      for (int ch = 0; ch < nch; ++ch) {
-        const int c0 = tl.bj * TN + ch * 16;
-        const int b = ch & 1;
-        if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
-                                    kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        ec.xphase ^= 1u << b;
-        uint32_t v[16];
-        ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(ch * 16), v);
-        ptx::tmem_ld_wait();
-        const uint8_t* xi = ec.buf + b * 2048;
-        float f[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 x = *reinterpret_cast<const float4*>(xi + ptx::sw64_off(lane, i));
-          f[4 * i + 0] = s * fmaf(ar, x.x, __uint_as_float(v[4 * i + 0]));
-          f[4 * i + 1] = s * fmaf(ar, x.y, __uint_as_float(v[4 * i + 1]));
-          f[4 * i + 2] = s * fmaf(ar, x.z, __uint_as_float(v[4 * i + 2]));
-          f[4 * i + 3] = s * fmaf(ar, x.w, __uint_as_float(v[4 * i + 3]));
-        }
-        ptx::fence_async_smem();
-        if (lane == 0) ptx::bulk_wait_read_all();
-        __syncwarp();
-        if (ch + 2 < nch) gemm_prefetch(p, G, tl, ec, b, c0 + 32, r0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float4*>(xo + ptx::sw64_off(lane, i)) =
-              make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-        if (G.out_b) {
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            uint4 u;
-            u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
-            u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
-            u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
-            u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
-            *reinterpret_cast<uint4*>(xbo + ptx::sw32_off(lane, i)) = u;
-          }
-        }
-        ptx::fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && r0 < G.m) {  // a box that starts past the last row is not stored
-          ptx::tma_store_4d(&p.map_c[tl.g], xo, c0, r0, tl.mat, G.buf_out);
-          if (G.out_b) ptx::tma_store_4d(&p.map_d[tl.g], xbo, c0, r0, tl.mat, G.buf_out);
-          ptx::bulk_commit();
-        }
-      }
-      if (!ok) {
-        // let the X prefetches in flight land before the CTA can exit
-        for (int b = 0; b < 2; ++b) wait_drain(&ec.xfull[b], (ec.xphase >> b) & 1u);
-        break;
-      }
+#ifdef MUON_TC_PROFILE
+    if (ec.lane == 0) TC_PROF_ADD(4, t_t);
+#endif
+    if (ok) {
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(ec.quarter * 32) << 16) + (uint32_t)(acc * TN);
+      if (kGram) gram_tile_epilogue(p, G, tl, ec, tbase, r0);
+      else ok = gemm_tile_epilogue(p, G, tl, ec, tbase, r0, cnt, abort);
+    }
+    if (!ok) {
+      // let this warp's X prefetches in flight land before the CTA can exit
+      if (!kGram)
+        for (int b = 0; b < 2; ++b)
+          if (b < cnt) wait_drain(&ec.xfull[b], (ec.xphase >> b) & 1u);
+      break;
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(&tempty[acc]);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
-  if (lane == 0) ptx::bulk_wait_all();
+  if (ec.lane == 0) ptx::bulk_wait_all();
   __syncwarp();
 }
 
 template <bool kGram>
-__global__ void __launch_bounds__(kThreads, 1) k_ns_tc(const __grid_constant__ PhaseParams p) {
+__global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_constant__ PhaseParams p) {
+  using C = Cfg<kGram>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint8_t* epi = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + EPI_BYTES);
+  uint8_t* epi = smem + C::kStages * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiWarps * C::kEpiWarpBytes);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* tfull = bars + 2 * C::kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* xfull = drain + 1;                 // 2 per epilogue warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 2 * C::kEpiWarps);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  TC_PROF_T0(t_cta);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], kEpiThreads);
+      ptx::mbar_init(&tempty[a], 32 * C::kEpiWarps);
     }
     ptx::mbar_init(drain, 1);
-    for (int i = 0; i < 8; ++i) ptx::mbar_init(&xfull[i], 1);
+    for (int i = 0; i < 2 * C::kEpiWarps; ++i) ptx::mbar_init(&xfull[i], 1);
     *abort = 0;
     ptx::fence_mbar_init();
     for (int g = 0; g < p.ngroups; ++g) {
@@ -521,12 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_tc(const __grid_constant__ P
     if (lane == 0) run_mma<kGram>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort);
     __syncwarp();
   } else {
+    const int e = warp - 2;
     EpiCtx ec;
-    ec.buf = epi + (warp - 2) * EPI_WARP_BYTES;
-    ec.xfull = xfull + 2 * (warp - 2);
+    ec.buf = epi + e * C::kEpiWarpBytes;
+    ec.xfull = xfull + 2 * e;
     ec.xphase = 0;
     ec.obuf = 0;
-    ec.quarter = warp & 3;
+    ec.quarter = warp & 3;   // TMEM lanes 32*(warp % 4) .. +31 are this warp's
+    ec.slice = e / 4;
     ec.lane = lane;
     run_epilogue<kGram>(p, tfull, tempty, tmem_base, ec, abort);
   }
@@ -537,21 +652,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_tc(const __grid_constant__ P
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
   }
+#ifdef MUON_TC_PROFILE
+  if (threadIdx.x == 0) TC_PROF_ADD(5, t_cta);
+#endif
 }
 
 template <bool kGram>
 int launch_tc(const PhaseParams& p, int grid, void* stream) {
+  using C = Cfg<kGram>;
   if (p.total_tiles == 0) return 0;
-  cudaError_t e = cudaFuncSetAttribute(k_ns_tc<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(k_ns_tc<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   if (grid > p.total_tiles) grid = p.total_tiles;
-  k_ns_tc<kGram><<<grid, kThreads, SMEM_BYTES, (cudaStream_t)stream>>>(p);
+  k_ns_tc<kGram><<<grid, C::kThreads, C::kSmemBytes, (cudaStream_t)stream>>>(p);
   return (int)cudaGetLastError();
 }
 
 }  // namespace
 
-int tc_smem_bytes() { return SMEM_BYTES; }
+int tc_smem_bytes() { return Cfg<true>::kSmemBytes; }
 int launch_gram_tc(const PhaseParams& p, int grid, void* stream) { return launch_tc<true>(p, grid, stream); }
 int launch_gemm_tc(const PhaseParams& p, int grid, void* stream) { return launch_tc<false>(p, grid, stream); }
 
