@@ -39,7 +39,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=None)
     ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunk", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -280,33 +281,34 @@ def run_gb300(args):
     phase["momentum_norm"]["gbs"] = k1_bytes / (phase["momentum_norm"]["ms_per_step"] / 1e3) / 1e9
     phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
 
-    # end to end through the C ABI with host buffers: H2D of G, W, M, the
-    # step, D2H of W and M, every step
+    # end to end with the state in pinned host memory: every step copies G,
+    # W, M in and W, M out, pipelined in chunks of whole matrices against the
+    # steps of other chunks (muon_newton_schulz_gb300.offload)
     e2e = None
     if not args.no_e2e:
+        from muon_newton_schulz_gb300.offload import HostOffloadedMuon
         Wh = [x.cpu().pin_memory() for x in Ws]
         Gh = [x.cpu().pin_memory() for x in Gs]
         Mh = [x.cpu().pin_memory() for x in Ms]
         h2d = sum(x.numel() * x.element_size() for x in Wh + Gh + Mh)
         d2h = sum(x.numel() * x.element_size() for x in Wh + Mh)
+        off = HostOffloadedMuon(local, chunk=args.e2e_chunk, slots=3, mode=mode)
+        off.step(Wh, Gh, Mh, lrs)           # warm-up: allocates the slot buffers
         torch.cuda.synchronize(dev)
         barrier()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            for hsrc, d in zip(Wh + Gh + Mh, Ws + Gs + Ms):
-                d.copy_(hsrc, non_blocking=True)
-            step()
-            for d, hdst in zip(Ws + Ms, Wh + Mh):
-                hdst.copy_(d, non_blocking=True)
-            torch.cuda.synchronize(dev)
+            off.step(Wh, Gh, Mh, lrs)
+        torch.cuda.synchronize(dev)
         dt = (time.perf_counter() - t0) / args.e2e_steps
+        off.close()
         if world > 1:
             import torch.distributed as dist
             t = torch.tensor([dt], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             dt = float(t.item())
         e2e = {"value": total_mats / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": dt * 1e3}
+               "ms_per_step": dt * 1e3, "pipeline": f"chunks of {args.e2e_chunk} matrices, 3 device slots"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
