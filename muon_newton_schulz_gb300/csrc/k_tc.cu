@@ -1,26 +1,35 @@
 // Tensor-core Newton-Schulz phases for sm_103a: tcgen05 UMMA with TMEM
 // accumulators fed by TMA, in one persistent, warp-specialised kernel that is
-// instantiated twice:
+// instantiated for two products:
 //
 //   Gram (kGram = true):  C = alpha * P P^T (+ coef_prev * prev)
 //       P is X (m x n, K = n) for A = X X^T, or A (m x m, K = m) for A A^T.
-//       Only 128 x 256 output tiles that reach the upper triangle are
-//       computed ("compute only the upper triangle of X X^T",
-//       jsqmd.com/news/1098463, section 4.2); each element (r, c), r <= c,
-//       is written to (r, c) and (c, r), so the result is exactly symmetric.
+//       Only output tiles that reach the upper triangle are computed
+//       ("compute only the upper triangle of X X^T", jsqmd.com/news/1098463,
+//       section 4.2); each element (r, c), r <= c, is written to (r, c) and
+//       (c, r), so the result is exactly symmetric.
 //   GEMM (kGram = false): X' = s * ((a + d) X + Bm X), Bm = b A + c A^2 (m x m)
 //       and d its fp32 per-row diagonal term.  The left operand is K-major
 //       (rows of Bm), the right one MN-major (rows of X), so no transposed
 //       copy of X is ever made.
 //
-// One CTA per SM walks a flattened list of (group, matrix, tile) entries with
-// a static stride (tile t -> CTA t mod grid): deterministic, and one launch
-// covers the whole ragged batch.  Warp 0 issues TMA loads into a shared-memory
-// ring, warp 1 issues the MMAs (128 x 256 x 16 per instruction) into one of
-// two TMEM accumulators (2 x 256 columns), and the epilogue warps drain the
-// other accumulator, so the epilogue of tile t overlaps the MMAs of tile t + 1.
-// Epilogue data moves through swizzled shared-memory staging with TMA loads
-// (the fp32 X tile, prefetched while the MMAs run) and TMA stores.
+// and for two tile shapes:
+//
+//   kPair = false: one CTA per SM computes 128 x 256 tiles with
+//       tcgen05.mma.cta_group::1 (M = 128, N = 256).
+//   kPair = true: a cluster of two CTAs on two SMs computes 256 x 256 tiles
+//       with tcgen05.mma.cta_group::2 (M = 256, N = 256): each CTA loads 128
+//       rows of the left operand and 128 columns of the right one, so a stage
+//       is 32 KiB instead of 48 and six stages fit; the even CTA issues the
+//       MMAs, and the odd CTA's copies complete on the even CTA's barriers.
+//
+// Tiles of all matrices of a launch form one flattened list walked with a
+// static stride (deterministic; one launch per phase covers the whole ragged
+// batch).  Warp 0 issues TMA loads into a shared-memory ring, warp 1 issues
+// the MMAs into one of two TMEM accumulators (2 x 256 columns), and the
+// epilogue warps drain the other accumulator through swizzled shared-memory
+// staging with TMA loads and stores, so the epilogue of tile t overlaps the
+// MMAs of tile t + 1.
 //
 // Every wait is bounded (one second): on a time-out the kernel records the
 // role in the status word, lets its copies and MMAs in flight finish, frees
@@ -28,11 +37,14 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <cstdio>
+
 #include "muon_internal.h"
 #include "ptx_sm100.cuh"
 
-// Pipeline shape of each instantiation (ring stages, epilogue warps, output
-// staging buffers of the GEMM epilogue).  Defaults are the measured best.
+// Pipeline shape of the single-CTA instantiations (ring stages, epilogue
+// warps, output staging buffers of the GEMM epilogue).  Defaults are the
+// measured best.
 #ifndef MUON_GRAM_STAGES
 #define MUON_GRAM_STAGES 4
 #endif
@@ -48,34 +60,39 @@
 #ifndef MUON_GEMM_OUT_BUFS
 #define MUON_GEMM_OUT_BUFS 1
 #endif
+#ifndef MUON_PAIR_STAGES
+#define MUON_PAIR_STAGES 6
+#endif
 
 namespace muon {
 
 namespace {
 
-constexpr int TM = kTcM;                    // 128 rows per tile (UMMA M)
+constexpr int TC = kTcM;                    // 128 rows per CTA (UMMA M per CTA)
 constexpr int TN = kTcN;                    // 256 columns per tile (UMMA N)
 constexpr int TK = kTcK;                    // 64 bf16 = 128 bytes = one swizzle row
 constexpr int UK = 16;                      // K per UMMA instruction
-constexpr int A_BYTES = TM * TK * 2;        // 16 KiB
-constexpr int B_BYTES = TN * TK * 2;        // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = TC * TK * 2;        // 16 KiB: 128 rows of the left operand
 constexpr int TMEM_COLS = 2 * TN;           // two fp32 accumulators
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kSmemLimit = 232448;          // 227 KiB per CTA
 
-template <bool kGram>
+template <bool kGram, bool kPair>
 struct Cfg {
-  static constexpr int kStages = kGram ? MUON_GRAM_STAGES : MUON_GEMM_STAGES;
-  static constexpr int kEpiWarps = kGram ? MUON_GRAM_EPI_WARPS : MUON_GEMM_EPI_WARPS;
-  static constexpr int kOutBufs = kGram ? 2 : MUON_GEMM_OUT_BUFS;
+  static constexpr int kStages = kPair ? MUON_PAIR_STAGES : (kGram ? MUON_GRAM_STAGES : MUON_GEMM_STAGES);
+  static constexpr int kEpiWarps = kPair ? 4 : (kGram ? MUON_GRAM_EPI_WARPS : MUON_GEMM_EPI_WARPS);
+  static constexpr int kOutBufs = kGram ? 2 : (kPair ? 1 : MUON_GEMM_OUT_BUFS);
   static constexpr int kSlices = kEpiWarps / 4;   // epilogue warps per TMEM lane quarter
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kTileM = kPair ? 2 * TC : TC;        // rows of an output tile
+  static constexpr int kBCols = kPair ? TN / 2 : TN;        // right-operand rows/columns per CTA
+  static constexpr int kBBytes = kBCols * TK * 2;
+  static constexpr int kStageBytes = A_BYTES + kBBytes;
   // Gram: row-major and transposed 32x32 bf16 blocks, double-buffered (8 KiB).
   // GEMM: two 2 KiB fp32 input buffers, then kOutBufs x (2 KiB fp32 + 1 KiB bf16).
   static constexpr int kEpiWarpBytes = kGram ? 8192 : (kOutBufs == 1 ? 8192 : 10240);
   static constexpr int kBarBytes = 512;
-  static constexpr int kSmemBytes = 1024 + kStages * STAGE_BYTES + kEpiWarps * kEpiWarpBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kBarBytes;
   static_assert(kEpiWarps % 4 == 0, "epilogue warps come in groups of four (one per TMEM lane quarter)");
   static_assert(kOutBufs == 1 || kOutBufs == 2, "one or two output staging buffers");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory over the per-CTA limit");
@@ -97,6 +114,11 @@ struct Tile { int g, mat, bi, bj; };
 #define TC_PROF_ADD(slot, v)
 #endif
 
+// Flattened tile t -> (group, matrix, row block, column block).  Gram tiles
+// are the upper ones: for 128 x 256 tiles, column block bj (256 wide) needs
+// row blocks bi < 2 bj + 2 (rows start before the block's last column); for
+// 256 x 256 tiles, bi <= bj.
+template <bool kPair>
 __device__ __forceinline__ Tile decode_tile(const PhaseParams& p, int t, bool gram) {
   int g = 0;
   while (g + 1 < p.ngroups && t >= p.g[g + 1].tile_begin) ++g;
@@ -107,11 +129,9 @@ __device__ __forceinline__ Tile decode_tile(const PhaseParams& p, int t, bool gr
   tl.mat = local / G.tiles_per_mat;
   int r = local - tl.mat * G.tiles_per_mat;
   if (gram) {
-    // column block bj (256 wide) needs row blocks bi (128 high) with
-    // 128*bi < 256*(bj+1), i.e. bi <= 2*bj + 1
     int bj = 0;
     while (true) {
-      const int cnt = min(2 * bj + 2, G.ni);
+      const int cnt = kPair ? bj + 1 : min(2 * bj + 2, G.ni);
       if (r < cnt) break;
       r -= cnt;
       ++bj;
@@ -134,72 +154,106 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-template <bool kGram>
-__device__ __forceinline__ void run_producer(const PhaseParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                             volatile int* abort) {
-  constexpr int S = Cfg<kGram>::kStages;
+template <bool kPair>
+__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                          uint32_t code) {
+  if (kPair) return ptx::mbar_wait_bounded_cluster(bar, parity, abort, status, code, kWaitLimitNs);
+  return ptx::mbar_wait_bounded(bar, parity, abort, status, code, kWaitLimitNs);
+}
+
+struct PairInfo {
+  int rank;      // 0 or 1 within the pair (0 when single-CTA)
+  int unit;      // this CTA's (or pair's) index in the persistent grid
+  int nunits;    // number of CTAs (or pairs)
+};
+
+template <bool kGram, bool kPair>
+__device__ __forceinline__ void run_producer(const PhaseParams& p, const PairInfo& pi, uint8_t* smem,
+                                             uint64_t* full, uint64_t* empty, volatile int* abort) {
+  using C = Cfg<kGram, kPair>;
+  constexpr int S = C::kStages;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t outstanding = 0, fill_parity = 0;
   bool ok = true;
-  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
-    const Tile tl = decode_tile(p, t, kGram);
+  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits) {
+    const Tile tl = decode_tile<kPair>(p, t, kGram);
     const PhaseGroup& G = p.g[tl.g];
     const int nk = (G.K + TK - 1) / TK;
     const CUtensorMap* ma = &p.map_a[tl.g];
     const CUtensorMap* mb = &p.map_b[tl.g];
+    const int arow = tl.bi * C::kTileM + TC * pi.rank;     // this CTA's left-operand rows
+    const int bcol = tl.bj * TN + C::kBCols * pi.rank;     // this CTA's right-operand rows/columns
     for (int kb = 0; kb < nk; ++kb) {
       TC_PROF_T0(t_e);
-      if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort, p.status, kStatusTimeoutProducer,
-                                  kWaitLimitNs)) {
+      if (!wait_role<false>(&empty[stage], phase ^ 1u, abort, p.status, kStatusTimeoutProducer)) {
         ok = false;
         break;
       }
       TC_PROF_ADD(3, t_e);
       outstanding &= ~(1u << stage);
-      uint8_t* sa = smem + stage * STAGE_BYTES;
+      uint8_t* sa = smem + stage * C::kStageBytes;
       uint8_t* sb = sa + A_BYTES;
-      ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
       const int k0 = kb * TK;
-      if (kGram) {
-        ptx::tma_load_4d(sa, ma, k0, tl.bi * TM, tl.mat, G.buf_in, &full[stage]);
-        ptx::tma_load_4d(sb, ma, k0, tl.bj * TN, tl.mat, G.buf_in, &full[stage]);
-        ptx::tma_load_4d(sb + A_BYTES, ma, k0, tl.bj * TN + TM, tl.mat, G.buf_in, &full[stage]);
-      } else {
-        ptx::tma_load_4d(sa, ma, k0, tl.bi * TM, tl.mat, 0, &full[stage]);
+      if (!kPair || pi.rank == 0) {
+        // the even CTA's barrier counts the bytes of both CTAs of a pair
+        ptx::mbar_arrive_expect_tx(&full[stage], (kPair ? 2 : 1) * C::kStageBytes);
+        if (kGram) {
+          ptx::tma_load_4d(sa, ma, k0, arow, tl.mat, G.buf_in, &full[stage]);
 #pragma unroll
-        for (int q = 0; q < TN / 64; ++q)
-          ptx::tma_load_4d(sb + q * (64 * TK * 2), mb, tl.bj * TN + 64 * q, k0, tl.mat, G.buf_in, &full[stage]);
+          for (int q = 0; q < C::kBCols / TC; ++q)
+            ptx::tma_load_4d(sb + q * A_BYTES, ma, k0, bcol + TC * q, tl.mat, G.buf_in, &full[stage]);
+        } else {
+          ptx::tma_load_4d(sa, ma, k0, arow, tl.mat, 0, &full[stage]);
+#pragma unroll
+          for (int q = 0; q < C::kBCols / 64; ++q)
+            ptx::tma_load_4d(sb + q * (64 * TK * 2), mb, bcol + 64 * q, k0, tl.mat, G.buf_in, &full[stage]);
+        }
+      } else {
+        // odd CTA: its copies land in its own shared memory and complete on
+        // the even CTA's barrier of the same stage
+        const uint32_t bar = ptx::mapa(ptx::smem_u32(&full[stage]), 0);
+        if (kGram) {
+          ptx::tma_load_4d_pair(sa, ma, k0, arow, tl.mat, G.buf_in, bar);
+          ptx::tma_load_4d_pair(sb, ma, k0, bcol, tl.mat, G.buf_in, bar);
+        } else {
+          ptx::tma_load_4d_pair(sa, ma, k0, arow, tl.mat, 0, bar);
+#pragma unroll
+          for (int q = 0; q < C::kBCols / 64; ++q)
+            ptx::tma_load_4d_pair(sb + q * (64 * TK * 2), mb, bcol + 64 * q, k0, tl.mat, G.buf_in, bar);
+        }
       }
       outstanding |= 1u << stage;
       fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == S) { stage = 0; phase ^= 1u; }
     }
   }
-  if (!ok) {
-    // let every copy this thread issued land before the CTA can exit
+  if (!ok && (!kPair || pi.rank == 0)) {
+    // let every copy issued (by this CTA, and by the odd CTA of a pair,
+    // whose copies complete on these barriers) land before the CTAs exit
     for (int s = 0; s < S; ++s)
       if ((outstanding >> s) & 1u)
         if (!wait_drain(&full[s], (fill_parity >> s) & 1u) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
   }
 }
 
-template <bool kGram>
-__device__ __forceinline__ void run_mma(const PhaseParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                        uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
-                                        volatile int* abort) {
-  constexpr int S = Cfg<kGram>::kStages;
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(TM, TN, !kGram);
+template <bool kGram, bool kPair>
+__device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi, uint8_t* smem, uint64_t* full,
+                                        uint64_t* empty, uint64_t* tfull, uint64_t* tempty, uint64_t* drain,
+                                        uint32_t tmem_base, volatile int* abort) {
+  using C = Cfg<kGram, kPair>;
+  constexpr int S = C::kStages;
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(C::kTileM, TN, !kGram);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true, issued = false;
-  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
-    const Tile tl = decode_tile(p, t, kGram);
+  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits) {
+    const Tile tl = decode_tile<kPair>(p, t, kGram);
     const int nk = (p.g[tl.g].K + TK - 1) / TK;
     TC_PROF_T0(t_a);
-    if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort, p.status, kStatusTimeoutMma, kWaitLimitNs)) {
+    if (!wait_role<kPair>(&tempty[acc], acc_phase ^ 1u, abort, p.status, kStatusTimeoutMma)) {
       ok = false;
       break;
     }
@@ -208,13 +262,13 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, uint8_t* smem, uin
     const uint32_t d = tmem_base + (uint32_t)(acc * TN);
     for (int kb = 0; kb < nk; ++kb) {
       TC_PROF_T0(t_f);
-      if (!ptx::mbar_wait_bounded(&full[stage], phase, abort, p.status, kStatusTimeoutMma, kWaitLimitNs)) {
+      if (!wait_role<false>(&full[stage], phase, abort, p.status, kStatusTimeoutMma)) {
         ok = false;
         break;
       }
       TC_PROF_ADD(1, t_f);
       ptx::tc_fence_after();
-      const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
+      const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
       const uint32_t sb = sa + A_BYTES;
 #pragma unroll
       for (int kk = 0; kk < TK / UK; ++kk) {
@@ -229,19 +283,23 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, uint8_t* smem, uin
           // 8-row K groups 1024 B apart (SBO); UK rows of K = 2 KiB.
           bd = ptx::smem_desc(sb + kk * UK * 128, 64 * TK * 2, 1024);
         }
-        ptx::umma_f16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        if (kPair) ptx::umma_f16_pair(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        else ptx::umma_f16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
       }
-      ptx::umma_commit(&empty[stage]);
+      if (kPair) ptx::umma_commit_pair_mc(&empty[stage], 0x3);   // frees the stage in both CTAs
+      else ptx::umma_commit(&empty[stage]);
       issued = true;
       if (++stage == S) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    ptx::umma_commit(&tfull[acc]);
+    if (kPair) ptx::umma_commit_pair_mc(&tfull[acc], 0x3);
+    else ptx::umma_commit(&tfull[acc]);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
   if (!ok && issued) {
-    ptx::umma_commit(drain);
+    if (kPair) ptx::umma_commit_pair_mc(drain, 0x1);
+    else ptx::umma_commit(drain);
     if (!wait_drain(drain, 0) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
   }
 }
@@ -257,7 +315,9 @@ struct EpiCtx {
   uint32_t xphase;     // parity bits of xfull[0..1]
   int obuf;            // next output staging buffer
   int quarter;         // TMEM lane quarter (warp index mod 4)
-  int slice;           // which of the kSlices column slices this warp drains
+  int slice;           // which of the column slices this warp drains
+  int nslices;
+  int out_bufs;        // GEMM output staging buffers (1 or 2)
   int lane;
 };
 
@@ -400,12 +460,11 @@ __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, con
 }
 
 __device__ __forceinline__ void gram_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
-                                                   EpiCtx& ec, uint32_t tbase, int r0) {
-  constexpr int kSl = Cfg<true>::kSlices;
+                                                   EpiCtx& ec, uint32_t tbase, int r0, int col0) {
   const int row = r0 + ec.lane;
 #pragma unroll 1
-  for (int ch = ec.slice; ch < TN / 32; ch += kSl) {
-    const int c0 = tl.bj * TN + ch * 32;
+  for (int ch = ec.slice; ch < TN / 32; ch += ec.nslices) {
+    const int c0 = col0 + ch * 32;
     if (c0 >= G.m) break;        // uniform across the warp
     if (c0 < r0) continue;       // wholly below the diagonal for this warp
     uint32_t v[32];
@@ -421,15 +480,15 @@ __device__ __forceinline__ void gram_tile_epilogue(const PhaseParams& p, const P
 // ---------------------------------------------------------------- GEMM epilogue
 
 // Per-warp GEMM staging: input X buffers at 0 / 2048 (32 rows x 16 fp32,
-// 64B swizzle); output buffer o holds X' fp32 at 4096 + 2048*o... laid out as
-// [fp32 x kOutBufs][bf16 x kOutBufs] (32 rows x 16 bf16, 32B swizzle).
+// 64B swizzle), then out_bufs fp32 X' buffers (same layout), then out_bufs
+// bf16 X' buffers (32 rows x 16 bf16, 32B swizzle).
 __device__ __forceinline__ uint8_t* gemm_xo(const EpiCtx& ec, int o) { return ec.buf + 4096 + 2048 * o; }
 __device__ __forceinline__ uint8_t* gemm_xbo(const EpiCtx& ec, int o) {
-  return ec.buf + 4096 + 2048 * Cfg<false>::kOutBufs + 1024 * o;
+  return ec.buf + 4096 + 2048 * ec.out_bufs + 1024 * o;
 }
 
-// chunk k of this warp covers columns 16 * (slice + k * kSlices) of the tile
-__device__ __forceinline__ int gemm_chunk_col(const EpiCtx& ec, int k) { return ec.slice + k * Cfg<false>::kSlices; }
+// chunk k of this warp covers columns 16 * (slice + k * nslices) of the tile
+__device__ __forceinline__ int gemm_chunk_col(const EpiCtx& ec, int k) { return ec.slice + k * ec.nslices; }
 
 __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
                                               EpiCtx& ec, int b, int c0, int r0) {
@@ -442,12 +501,11 @@ __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseG
 // One 16-column chunk: X' = s * ((a + d) * X + acc), written as fp32 (and
 // bf16) through the staging buffers.  Returns false on a time-out.
 __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, EpiCtx& ec,
-                                           int k, int cnt, int r0, float s, float ar, const uint32_t (&v)[16],
-                                           volatile int* abort) {
-  constexpr int kSl = Cfg<false>::kSlices;
+                                           int col0, int k, int cnt, int r0, float s, float ar,
+                                           const uint32_t (&v)[16], volatile int* abort) {
   const int lane = ec.lane;
   const int b = k & 1;
-  const int c0 = tl.bj * TN + 16 * gemm_chunk_col(ec, k);
+  const int c0 = col0 + 16 * gemm_chunk_col(ec, k);
   if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
                               kWaitLimitNs))
     return false;
@@ -464,12 +522,12 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   }
   ptx::fence_async_smem();
   if (lane == 0) {
-    if (Cfg<false>::kOutBufs == 2) ptx::bulk_wait_read_1();
+    if (ec.out_bufs == 2) ptx::bulk_wait_read_1();
     else ptx::bulk_wait_read_all();
   }
   __syncwarp();
-  if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * kSl, r0);
-  const int o = Cfg<false>::kOutBufs == 2 ? ec.obuf : 0;
+  if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * ec.nslices, r0);
+  const int o = ec.out_bufs == 2 ? ec.obuf : 0;
   uint8_t* xo = gemm_xo(ec, o);
   uint8_t* xbo = gemm_xbo(ec, o);
 #pragma unroll
@@ -500,7 +558,8 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
 // The GEMM tile's epilogue for this warp; TMEM loads of chunk k + 1 are in
 // flight while chunk k is processed.
 __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
-                                                   EpiCtx& ec, uint32_t tbase, int r0, int cnt, volatile int* abort) {
+                                                   EpiCtx& ec, uint32_t tbase, int r0, int col0, int cnt,
+                                                   volatile int* abort) {
   const int row = r0 + ec.lane;
   const float s = p.scale ? p.scale[G.first + tl.mat] : 1.f;
   // a plus this row's fp32 diagonal term of B (residual or exact diagonal)
@@ -513,7 +572,7 @@ __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const P
   for (int k = 0; k < cnt; k += 2) {
     const bool has1 = k + 1 < cnt;
     if (has1) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, k + 1)), vb);
-    if (!gemm_chunk(p, G, tl, ec, k, cnt, r0, s, ar, va, abort)) {
+    if (!gemm_chunk(p, G, tl, ec, col0, k, cnt, r0, s, ar, va, abort)) {
       if (has1) ptx::tmem_ld_wait_regs(vb);
       return false;
     }
@@ -521,7 +580,7 @@ __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const P
       ptx::tmem_ld_wait_regs(vb);
       const bool has2 = k + 2 < cnt;
       if (has2) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, k + 2)), va);
-      const bool okb = gemm_chunk(p, G, tl, ec, k + 1, cnt, r0, s, ar, vb, abort);
+      const bool okb = gemm_chunk(p, G, tl, ec, col0, k + 1, cnt, r0, s, ar, vb, abort);
       if (has2) ptx::tmem_ld_wait_regs(va);
       if (!okb) return false;
     }
@@ -529,35 +588,34 @@ __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const P
   return true;
 }
 
-template <bool kGram>
-__device__ __forceinline__ void run_epilogue(const PhaseParams& p, uint64_t* tfull, uint64_t* tempty,
-                                             uint32_t tmem_base, EpiCtx& ec, volatile int* abort) {
-  constexpr int kSl = Cfg<kGram>::kSlices;
+template <bool kGram, bool kPair>
+__device__ __forceinline__ void run_epilogue(const PhaseParams& p, const PairInfo& pi, uint64_t* tfull,
+                                             uint64_t* tempty, uint32_t tmem_base, EpiCtx& ec, volatile int* abort) {
+  using C = Cfg<kGram, kPair>;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true;
-  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
-    const Tile tl = decode_tile(p, t, kGram);
+  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits) {
+    const Tile tl = decode_tile<kPair>(p, t, kGram);
     const PhaseGroup& G = p.g[tl.g];
-    const int r0 = tl.bi * TM + ec.quarter * 32;   // first row of this warp
+    const int r0 = tl.bi * C::kTileM + TC * pi.rank + ec.quarter * 32;   // first row of this warp
+    const int col0 = tl.bj * TN;
     int cnt = 0;
     if (!kGram) {
-      const int nch = min(TN / 16, (G.n - tl.bj * TN + 15) / 16);
-      cnt = nch > ec.slice ? (nch - ec.slice + kSl - 1) / kSl : 0;
-      for (int k = 0; k < 2 && k < cnt; ++k) gemm_prefetch(p, G, tl, ec, k, tl.bj * TN + 16 * gemm_chunk_col(ec, k), r0);
+      const int nch = min(TN / 16, (G.n - col0 + 15) / 16);
+      cnt = nch > ec.slice ? (nch - ec.slice + ec.nslices - 1) / ec.nslices : 0;
+      for (int k = 0; k < 2 && k < cnt; ++k) gemm_prefetch(p, G, tl, ec, k, col0 + 16 * gemm_chunk_col(ec, k), r0);
     }
     TC_PROF_T0(t_t);
-    if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, abort, p.status, kStatusTimeoutEpilogue, kWaitLimitNs)) {
-      ok = false;
-    }
+    if (!wait_role<false>(&tfull[acc], acc_phase, abort, p.status, kStatusTimeoutEpilogue)) ok = false;
 #ifdef MUON_TC_PROFILE
     if (ec.lane == 0) TC_PROF_ADD(4, t_t);
 #endif
     if (ok) {
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(ec.quarter * 32) << 16) + (uint32_t)(acc * TN);
-      if (kGram) gram_tile_epilogue(p, G, tl, ec, tbase, r0);
-      else ok = gemm_tile_epilogue(p, G, tl, ec, tbase, r0, cnt, abort);
+      if (kGram) gram_tile_epilogue(p, G, tl, ec, tbase, r0, col0);
+      else ok = gemm_tile_epilogue(p, G, tl, ec, tbase, r0, col0, cnt, abort);
     }
     if (!ok) {
       // let this warp's X prefetches in flight land before the CTA can exit
@@ -567,7 +625,13 @@ __device__ __forceinline__ void run_epilogue(const PhaseParams& p, uint64_t* tfu
       break;
     }
     ptx::tc_fence_before();
-    ptx::mbar_arrive(&tempty[acc]);
+    if (kPair) {
+      // one arrival per warp, on the even CTA's barrier
+      __syncwarp();
+      if (ec.lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&tempty[acc]), 0));
+    } else {
+      ptx::mbar_arrive(&tempty[acc]);
+    }
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
@@ -575,13 +639,13 @@ __device__ __forceinline__ void run_epilogue(const PhaseParams& p, uint64_t* tfu
   __syncwarp();
 }
 
-template <bool kGram>
-__global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_constant__ PhaseParams p) {
-  using C = Cfg<kGram>;
+template <bool kGram, bool kPair>
+__device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
+  using C = Cfg<kGram, kPair>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint8_t* epi = smem + C::kStages * STAGE_BYTES;
+  uint8_t* epi = smem + C::kStages * C::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiWarps * C::kEpiWarpBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
@@ -594,6 +658,16 @@ __global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  PairInfo pi;
+  if (kPair) {
+    pi.rank = (int)ptx::cluster_ctarank();
+    pi.unit = blockIdx.x >> 1;
+    pi.nunits = gridDim.x >> 1;
+  } else {
+    pi.rank = 0;
+    pi.unit = blockIdx.x;
+    pi.nunits = gridDim.x;
+  }
   TC_PROF_T0(t_cta);
 
   if (threadIdx.x == 0) {
@@ -603,7 +677,7 @@ __global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 32 * C::kEpiWarps);
+      ptx::mbar_init(&tempty[a], kPair ? 2 * C::kEpiWarps : 32 * C::kEpiWarps);
     }
     ptx::mbar_init(drain, 1);
     for (int i = 0; i < 2 * C::kEpiWarps; ++i) ptx::mbar_init(&xfull[i], 1);
@@ -619,19 +693,26 @@ __global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_
     }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (kPair) {
+      ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if (kPair) ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrival
+  else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<kGram>(p, smem, full, empty, abort);
+    if (lane == 0) run_producer<kGram, kPair>(p, pi, smem, full, empty, abort);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<kGram>(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort);
+    if (lane == 0 && (!kPair || pi.rank == 0))
+      run_mma<kGram, kPair>(p, pi, smem, full, empty, tfull, tempty, drain, tmem_base, abort);
     __syncwarp();
   } else {
     const int e = warp - 2;
@@ -642,15 +723,19 @@ __global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_
     ec.obuf = 0;
     ec.quarter = warp & 3;   // TMEM lanes 32*(warp % 4) .. +31 are this warp's
     ec.slice = e / 4;
+    ec.nslices = C::kSlices;
+    ec.out_bufs = C::kOutBufs;
     ec.lane = lane;
-    run_epilogue<kGram>(p, tfull, tempty, tmem_base, ec, abort);
+    run_epilogue<kGram, kPair>(p, pi, tfull, tempty, tmem_base, ec, abort);
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  if (kPair) ptx::cluster_sync();   // no CTA leaves while its pair may still touch its memory
+  else __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    if (kPair) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else ptx::tmem_dealloc(tmem_base, TMEM_COLS);
   }
 #ifdef MUON_TC_PROFILE
   if (threadIdx.x == 0) TC_PROF_ADD(5, t_cta);
@@ -658,8 +743,19 @@ __global__ void __launch_bounds__(Cfg<kGram>::kThreads, 1) k_ns_tc(const __grid_
 }
 
 template <bool kGram>
+__global__ void __launch_bounds__(Cfg<kGram, false>::kThreads, 1) k_ns_tc(const __grid_constant__ PhaseParams p) {
+  ns_tc_body<kGram, false>(p);
+}
+
+template <bool kGram>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kGram, true>::kThreads, 1)
+    k_ns_tc_pair(const __grid_constant__ PhaseParams p) {
+  ns_tc_body<kGram, true>(p);
+}
+
+template <bool kGram>
 int launch_tc(const PhaseParams& p, int grid, void* stream) {
-  using C = Cfg<kGram>;
+  using C = Cfg<kGram, false>;
   if (p.total_tiles == 0) return 0;
   cudaError_t e = cudaFuncSetAttribute(k_ns_tc<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
@@ -668,10 +764,44 @@ int launch_tc(const PhaseParams& p, int grid, void* stream) {
   return (int)cudaGetLastError();
 }
 
+// Pairs: as many co-resident clusters of two as the device holds, capped by
+// the number of tiles.
+template <bool kGram>
+int launch_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
+  using C = Cfg<kGram, true>;
+  if (p.total_tiles == 0) return 0;
+  cudaError_t e =
+      cudaFuncSetAttribute(k_ns_tc_pair<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return (int)e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sm_count, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = (cudaStream_t)stream;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, k_ns_tc_pair<kGram>, &cfg);
+  if (e != cudaSuccess) return (int)e;
+  if (clusters <= 0) return (int)cudaErrorLaunchOutOfResources;
+  if (clusters > sm_count / 2) clusters = sm_count / 2;
+  if (clusters > p.total_tiles) clusters = p.total_tiles;
+#ifdef MUON_TC_PROFILE
+  fprintf(stderr, "k_ns_tc_pair<%d>: %d clusters of 2 for %d tiles (%d SMs)\n", (int)kGram, clusters, p.total_tiles,
+          sm_count);
+#endif
+  k_ns_tc_pair<kGram><<<2 * clusters, C::kThreads, C::kSmemBytes, (cudaStream_t)stream>>>(p);
+  return (int)cudaGetLastError();
+}
+
 }  // namespace
 
-int tc_smem_bytes() { return Cfg<true>::kSmemBytes; }
+int tc_smem_bytes() { return Cfg<true, false>::kSmemBytes; }
 int launch_gram_tc(const PhaseParams& p, int grid, void* stream) { return launch_tc<true>(p, grid, stream); }
 int launch_gemm_tc(const PhaseParams& p, int grid, void* stream) { return launch_tc<false>(p, grid, stream); }
+int launch_gram_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
+  return launch_tc_pair<true>(p, sm_count, stream);
+}
+int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
+  return launch_tc_pair<false>(p, sm_count, stream);
+}
 
 }  // namespace muon

@@ -254,7 +254,17 @@ bool encode_map(muon_handle h, CUtensorMap* map, void* base, uint64_t d0, uint64
 
 // Tile counts of one group for the kernel that will run the phase.
 void set_tiles(PhaseGroup& pg, bool gram, bool tc) {
-  if (tc) {
+  if (tc && muon::kUsePair) {
+    // CTA pairs: 256 x 256 tiles; Gram keeps the tiles with bi <= bj
+    pg.ni = (int32_t)cdiv(pg.m, 2 * muon::kTcM);
+    if (gram) {
+      pg.nj = pg.ni;
+      pg.tiles_per_mat = pg.ni * (pg.ni + 1) / 2;
+    } else {
+      pg.nj = (int32_t)cdiv(pg.n, muon::kTcN);
+      pg.tiles_per_mat = pg.ni * pg.nj;
+    }
+  } else if (tc) {
     pg.ni = (int32_t)cdiv(pg.m, muon::kTcM);
     if (gram) {
       pg.nj = (int32_t)cdiv(pg.m, muon::kTcN);
@@ -677,7 +687,9 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
         }
         pp->total_tiles = tiles;
         int rc;
-        if (bf16) rc = gram ? muon::launch_gram_tc(*pp, grid, stream) : muon::launch_gemm_tc(*pp, grid, stream);
+        if (bf16 && muon::kUsePair)
+          rc = gram ? muon::launch_gram_tc_pair(*pp, h->sm_count, stream) : muon::launch_gemm_tc_pair(*pp, h->sm_count, stream);
+        else if (bf16) rc = gram ? muon::launch_gram_tc(*pp, grid, stream) : muon::launch_gemm_tc(*pp, grid, stream);
         else rc = gram ? muon::launch_gram_f32(*pp, stream) : muon::launch_gemm_f32(*pp, stream);
         if ((st = launched(rc, gram ? "Gram kernel" : "GEMM kernel")) != MUON_OK) return st;
       }

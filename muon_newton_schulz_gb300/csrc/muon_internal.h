@@ -108,11 +108,21 @@ int launch_gram_f32(const PhaseParams& p, void* stream);
 int launch_gemm_f32(const PhaseParams& p, void* stream);
 int launch_gram_tc(const PhaseParams& p, int grid, void* stream);
 int launch_gemm_tc(const PhaseParams& p, int grid, void* stream);
+int launch_gram_tc_pair(const PhaseParams& p, int sm_count, void* stream);
+int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream);
 int tc_smem_bytes();
 
-// Tensor-core tile shape (used by the planner to count tiles).
+// Tensor-core tile shape (used by the planner to count tiles): a CTA covers
+// kTcM rows; a CTA pair (cta_group::2) covers 2 * kTcM rows.
 constexpr int kTcM = 128;
 constexpr int kTcN = 256;
 constexpr int kTcK = 64;
+
+// The Newton-Schulz phases run on CTA pairs (256 x 256 tiles) unless built
+// with -DMUON_USE_PAIR=0 (single CTAs, 128 x 256 tiles).
+#ifndef MUON_USE_PAIR
+#define MUON_USE_PAIR 1
+#endif
+constexpr bool kUsePair = MUON_USE_PAIR != 0;
 
 }  // namespace muon
