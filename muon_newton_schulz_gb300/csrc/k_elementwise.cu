@@ -43,11 +43,63 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
   return s;
 }
 
+// X storage: fp32 (validation mode) or a bf16 pair hi = bf16(x),
+// lo = bf16(x - hi) (tensor-core mode; hi is also the MMA operand).  x - hi
+// is exact in fp32 and hi + lo carries about 17 significant bits.
+__device__ __forceinline__ void store_x4(const EltMat& e, int64_t off, const float (&v)[4], int nvalid) {
+  if (e.xm0) {
+    if (nvalid == 4) {
+      *reinterpret_cast<float4*>(e.xm0 + off) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+      for (int q = 0; q < nvalid; ++q) e.xm0[off + q] = v[q];
+    }
+    return;
+  }
+  __nv_bfloat16 h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    h[q] = __float2bfloat16_rn(v[q]);
+    l[q] = __float2bfloat16_rn(v[q] - __bfloat162float(h[q]));
+  }
+  if (nvalid == 4) {
+    *reinterpret_cast<uint2*>(e.xhi0 + off) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(e.xlo0 + off) = *reinterpret_cast<const uint2*>(l);
+  } else {
+    for (int q = 0; q < nvalid; ++q) {
+      e.xhi0[off + q] = h[q];
+      e.xlo0[off + q] = l[q];
+    }
+  }
+}
+
+__device__ __forceinline__ void load_x4(const EltMat& e, int64_t off, float (&v)[4], int nvalid) {
+  if (e.xm_final) {
+    if (nvalid == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(e.xm_final + off);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      for (int q = 0; q < nvalid; ++q) v[q] = e.xm_final[off + q];
+    }
+    return;
+  }
+  if (nvalid == 4) {
+    const uint2 hu = *reinterpret_cast<const uint2*>(e.xhi_final + off);
+    const uint2 lu = *reinterpret_cast<const uint2*>(e.xlo_final + off);
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&hu);
+    const __nv_bfloat16* l = reinterpret_cast<const __nv_bfloat16*>(&lu);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __bfloat162float(h[q]) + __bfloat162float(l[q]);
+  } else {
+    for (int q = 0; q < nvalid; ++q)
+      v[q] = __bfloat162float(e.xhi_final[off + q]) + __bfloat162float(e.xlo_final[off + q]);
+  }
+}
+
 // ---------------------------------------------------------------- K1
 // M <- beta*M + G (fp32 fma, in place); X0 = M (or G + beta*M with Nesterov)
-// written in wide orientation as fp32 master and bf16 operand; one fp64 sum
-// of squares of X0 per tile.  The normalisation 1/(||X0||+eps) is not applied
-// here: it is folded into the first iteration's epilogues.
+// written in wide orientation (fp32, or as the bf16 hi/lo pair); one fp64
+// sum of squares of X0 per tile.  The normalisation 1/(||X0||+eps) is not
+// applied here: it is folded into the first iteration's epilogues.
 __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constant__ EltParams p) {
   __shared__ float tile[kT][kT + 1];
   __shared__ double red[kThreads / 32];
@@ -97,24 +149,7 @@ __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constan
         if (c + q < e.cols) e.M[(int64_t)r * e.ldm + c + q] = mm[q];
     }
     if (!e.tall) {
-      if (vec) {
-        *reinterpret_cast<float4*>(e.xm0 + (int64_t)r * e.ldx + c) = make_float4(x[0], x[1], x[2], x[3]);
-        if (e.xb0) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
-          __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(e.xb0 + (int64_t)r * e.ldx + c) = pk;
-        }
-      } else if (row_ok) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (c + q < e.cols) {
-            e.xm0[(int64_t)r * e.ldx + c + q] = x[q];
-            if (e.xb0) e.xb0[(int64_t)r * e.ldx + c + q] = __float2bfloat16_rn(x[q]);
-          }
-      }
+      if (row_ok) store_x4(e, (int64_t)r * e.ldx + c, x, vec ? 4 : max(0, min(4, e.cols - c)));
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q) tile[ty + 16 * k][tx * 4 + q] = x[q];
@@ -133,24 +168,7 @@ __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constan
       float v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) v[q] = tile[tx * 4 + q][ty + 16 * k];
-      if (xc + 3 < e.rows) {
-        *reinterpret_cast<float4*>(e.xm0 + (int64_t)xr * e.ldx + xc) = make_float4(v[0], v[1], v[2], v[3]);
-        if (e.xb0) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-          __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(e.xb0 + (int64_t)xr * e.ldx + xc) = pk;
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (xc + q < e.rows) {
-            e.xm0[(int64_t)xr * e.ldx + xc + q] = v[q];
-            if (e.xb0) e.xb0[(int64_t)xr * e.ldx + xc + q] = __float2bfloat16_rn(v[q]);
-          }
-      }
+      store_x4(e, (int64_t)xr * e.ldx + xc, v, max(0, min(4, e.rows - xc)));
     }
   }
 
@@ -190,16 +208,7 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ EltP
       const int xr = c0 + ty + 16 * k;
       const int xc = r0 + tx * 4;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (xr < e.cols) {
-        if (xc + 3 < e.rows) {
-          const float4 t = *reinterpret_cast<const float4*>(e.xm_final + (int64_t)xr * e.ldx + xc);
-          v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (xc + q < e.rows) v[q] = e.xm_final[(int64_t)xr * e.ldx + xc + q];
-        }
-      }
+      if (xr < e.cols) load_x4(e, (int64_t)xr * e.ldx + xc, v, max(0, min(4, e.rows - xc)));
 #pragma unroll
       for (int q = 0; q < 4; ++q) tile[tx * 4 + q][ty + 16 * k] = v[q];
     }
@@ -216,13 +225,8 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ EltP
     if (e.tall) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) o[q] = tile[ty + 16 * k][tx * 4 + q];
-    } else if (vec) {
-      const float4 t = *reinterpret_cast<const float4*>(e.xm_final + (int64_t)r * e.ldx + c);
-      o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
     } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (c + q < e.cols) o[q] = e.xm_final[(int64_t)r * e.ldx + c + q];
+      load_x4(e, (int64_t)r * e.ldx + c, o, vec ? 4 : max(0, min(4, e.cols - c)));
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) o[q] *= os;

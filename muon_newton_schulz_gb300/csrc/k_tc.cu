@@ -9,9 +9,9 @@
 //       section 4.2); each element (r, c), r <= c, is written to (r, c) and
 //       (c, r), so the result is exactly symmetric.
 //   GEMM (kGram = false): X' = s * ((a + d) X + Bm X), Bm = b A + c A^2 (m x m)
-//       and d its fp32 per-row diagonal term.  The left operand is K-major
-//       (rows of Bm), the right one MN-major (rows of X), so no transposed
-//       copy of X is ever made.
+//       and d its fp32 per-row diagonal term.  X is stored as a bf16 pair
+//       (hi, lo); hi is the right operand, read MN-major (rows of X), so no
+//       transposed copy of X is ever made.
 //
 // and for two tile shapes:
 //
@@ -58,10 +58,23 @@
 #define MUON_GEMM_EPI_WARPS 4
 #endif
 #ifndef MUON_GEMM_OUT_BUFS
-#define MUON_GEMM_OUT_BUFS 1
+#define MUON_GEMM_OUT_BUFS 2
 #endif
-#ifndef MUON_PAIR_STAGES
-#define MUON_PAIR_STAGES 6
+// ... and of the CTA-pair instantiations
+#ifndef MUON_PAIR_GRAM_STAGES
+#define MUON_PAIR_GRAM_STAGES 6
+#endif
+#ifndef MUON_PAIR_GEMM_STAGES
+#define MUON_PAIR_GEMM_STAGES 6
+#endif
+#ifndef MUON_PAIR_GRAM_EPI_WARPS
+#define MUON_PAIR_GRAM_EPI_WARPS 4
+#endif
+#ifndef MUON_PAIR_GEMM_EPI_WARPS
+#define MUON_PAIR_GEMM_EPI_WARPS 4
+#endif
+#ifndef MUON_PAIR_GEMM_OUT_BUFS
+#define MUON_PAIR_GEMM_OUT_BUFS 2
 #endif
 
 namespace muon {
@@ -79,9 +92,11 @@ constexpr int kSmemLimit = 232448;          // 227 KiB per CTA
 
 template <bool kGram, bool kPair>
 struct Cfg {
-  static constexpr int kStages = kPair ? MUON_PAIR_STAGES : (kGram ? MUON_GRAM_STAGES : MUON_GEMM_STAGES);
-  static constexpr int kEpiWarps = kPair ? 4 : (kGram ? MUON_GRAM_EPI_WARPS : MUON_GEMM_EPI_WARPS);
-  static constexpr int kOutBufs = kGram ? 2 : (kPair ? 1 : MUON_GEMM_OUT_BUFS);
+  static constexpr int kStages = kPair ? (kGram ? MUON_PAIR_GRAM_STAGES : MUON_PAIR_GEMM_STAGES)
+                                       : (kGram ? MUON_GRAM_STAGES : MUON_GEMM_STAGES);
+  static constexpr int kEpiWarps = kPair ? (kGram ? MUON_PAIR_GRAM_EPI_WARPS : MUON_PAIR_GEMM_EPI_WARPS)
+                                         : (kGram ? MUON_GRAM_EPI_WARPS : MUON_GEMM_EPI_WARPS);
+  static constexpr int kOutBufs = kGram ? 2 : (kPair ? MUON_PAIR_GEMM_OUT_BUFS : MUON_GEMM_OUT_BUFS);
   static constexpr int kSlices = kEpiWarps / 4;   // epilogue warps per TMEM lane quarter
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kTileM = kPair ? 2 * TC : TC;        // rows of an output tile
@@ -89,8 +104,8 @@ struct Cfg {
   static constexpr int kBBytes = kBCols * TK * 2;
   static constexpr int kStageBytes = A_BYTES + kBBytes;
   // Gram: row-major and transposed 32x32 bf16 blocks, double-buffered (8 KiB).
-  // GEMM: two 2 KiB fp32 input buffers, then kOutBufs x (2 KiB fp32 + 1 KiB bf16).
-  static constexpr int kEpiWarpBytes = kGram ? 8192 : (kOutBufs == 1 ? 8192 : 10240);
+  // GEMM: two 2 KiB input buffers and two 2 KiB output buffers (hi/lo pairs).
+  static constexpr int kEpiWarpBytes = 8192;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kBarBytes;
   static_assert(kEpiWarps % 4 == 0, "epilogue warps come in groups of four (one per TMEM lane quarter)");
@@ -479,13 +494,12 @@ __device__ __forceinline__ void gram_tile_epilogue(const PhaseParams& p, const P
 
 // ---------------------------------------------------------------- GEMM epilogue
 
-// Per-warp GEMM staging: input X buffers at 0 / 2048 (32 rows x 16 fp32,
-// 64B swizzle), then out_bufs fp32 X' buffers (same layout), then out_bufs
-// bf16 X' buffers (32 rows x 16 bf16, 32B swizzle).
-__device__ __forceinline__ uint8_t* gemm_xo(const EpiCtx& ec, int o) { return ec.buf + 4096 + 2048 * o; }
-__device__ __forceinline__ uint8_t* gemm_xbo(const EpiCtx& ec, int o) {
-  return ec.buf + 4096 + 2048 * ec.out_bufs + 1024 * o;
-}
+// X is kept as a bf16 pair hi = bf16(x), lo = bf16(x - hi) (about 17
+// significant bits); hi is also the MMA operand of the next iteration.
+// Per-warp GEMM staging, each box 32 rows x 16 bf16 (32B swizzle, 1 KiB):
+// input buffer b holds hi at 2048 b and lo at 2048 b + 1024; output buffer o
+// holds hi' at 4096 + 2048 o and lo' at 4096 + 2048 o + 1024.
+__device__ __forceinline__ uint8_t* gemm_out(const EpiCtx& ec, int o) { return ec.buf + 4096 + 2048 * o; }
 
 // chunk k of this warp covers columns 16 * (slice + k * nslices) of the tile
 __device__ __forceinline__ int gemm_chunk_col(const EpiCtx& ec, int k) { return ec.slice + k * ec.nslices; }
@@ -495,11 +509,22 @@ __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseG
   if (ec.lane == 0) {
     ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2048);
     ptx::tma_load_4d(ec.buf + b * 2048, &p.map_c[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
+    ptx::tma_load_4d(ec.buf + b * 2048 + 1024, &p.map_d[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
   }
 }
 
-// One 16-column chunk: X' = s * ((a + d) * X + acc), written as fp32 (and
-// bf16) through the staging buffers.  Returns false on a time-out.
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+    f[2 * h] = __low2float(b2);
+    f[2 * h + 1] = __high2float(b2);
+  }
+}
+
+// One 16-column chunk: X' = s * ((a + d) * X + acc), written as the bf16
+// hi/lo pair through the staging buffers.  Returns false on a time-out.
 __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, EpiCtx& ec,
                                            int col0, int k, int cnt, int r0, float s, float ar,
                                            const uint32_t (&v)[16], volatile int* abort) {
@@ -510,15 +535,16 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
                               kWaitLimitNs))
     return false;
   ec.xphase ^= 1u << b;
-  const uint8_t* xi = ec.buf + b * 2048;
+  const uint8_t* xh = ec.buf + b * 2048;
+  const uint8_t* xl = xh + 1024;
   float f[16];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 x = *reinterpret_cast<const float4*>(xi + ptx::sw64_off(lane, i));
-    f[4 * i + 0] = s * fmaf(ar, x.x, __uint_as_float(v[4 * i + 0]));
-    f[4 * i + 1] = s * fmaf(ar, x.y, __uint_as_float(v[4 * i + 1]));
-    f[4 * i + 2] = s * fmaf(ar, x.z, __uint_as_float(v[4 * i + 2]));
-    f[4 * i + 3] = s * fmaf(ar, x.w, __uint_as_float(v[4 * i + 3]));
+  for (int i = 0; i < 2; ++i) {
+    float hv[8], lv[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(xh + ptx::sw32_off(lane, i)), hv);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(xl + ptx::sw32_off(lane, i)), lv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[8 * i + j] = s * fmaf(ar, hv[j] + lv[j], __uint_as_float(v[8 * i + j]));
   }
   ptx::fence_async_smem();
   if (lane == 0) {
@@ -528,27 +554,27 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   __syncwarp();
   if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * ec.nslices, r0);
   const int o = ec.out_bufs == 2 ? ec.obuf : 0;
-  uint8_t* xo = gemm_xo(ec, o);
-  uint8_t* xbo = gemm_xbo(ec, o);
+  uint8_t* oh = gemm_out(ec, o);
+  uint8_t* ol = oh + 1024;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<float4*>(xo + ptx::sw64_off(lane, i)) = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-  if (G.out_b) {
+  for (int i = 0; i < 2; ++i) {
+    uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      uint4 u;
-      u.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
-      u.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
-      u.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
-      u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
-      *reinterpret_cast<uint4*>(xbo + ptx::sw32_off(lane, i)) = u;
+    for (int j = 0; j < 4; ++j) {
+      const float x0 = f[8 * i + 2 * j], x1 = f[8 * i + 2 * j + 1];
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+      const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
+      hw[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      lw[j] = *reinterpret_cast<const uint32_t*>(&l2);
     }
+    *reinterpret_cast<uint4*>(oh + ptx::sw32_off(lane, i)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(ol + ptx::sw32_off(lane, i)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
   ptx::fence_async_smem();
   __syncwarp();
   if (lane == 0 && r0 < G.m) {  // a box that starts past the last row is not stored
-    ptx::tma_store_4d(&p.map_c[tl.g], xo, c0, r0, tl.mat, G.buf_out);
-    if (G.out_b) ptx::tma_store_4d(&p.map_d[tl.g], xbo, c0, r0, tl.mat, G.buf_out);
+    ptx::tma_store_4d(&p.map_c[tl.g], oh, c0, r0, tl.mat, G.buf_out);
+    ptx::tma_store_4d(&p.map_d[tl.g], ol, c0, r0, tl.mat, G.buf_out);
   }
   if (lane == 0) ptx::bulk_commit();   // one group per chunk (possibly empty)
   ec.obuf ^= 1;

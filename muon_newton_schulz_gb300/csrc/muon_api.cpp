@@ -214,8 +214,10 @@ Plan build_plan(const muon_config& cfg, const muon_matrix_desc* d, int n) {
   for (GroupPlan& G : P.groups) {
     const size_t xel = (size_t)G.count * G.m * G.ldx;
     const size_t ael = (size_t)G.count * G.m * G.lda;
+    // X ping-pong: fp32 (validation mode), or bf16 hi at off_xm and bf16 lo
+    // at off_xb (tensor-core mode)
     G.off_xm = off;
-    off = align_up(off + 2 * xel * sizeof(float), 1024);
+    off = align_up(off + 2 * xel * (bf16 ? 2 : 4), 1024);
     if (bf16) {
       G.off_xb = off;
       off = align_up(off + 2 * xel * 2, 1024);
@@ -507,10 +509,15 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
     return MUON_OK;
   };
 
+  // X of matrix k of a group, ping-pong buffer `buf`: fp32 in validation
+  // mode; the bf16 pair (hi, lo) in tensor-core mode
   auto xm_ptr = [&](const GroupPlan& G, int buf, int k) -> float* {
     return reinterpret_cast<float*>(base + G.off_xm) + ((size_t)buf * G.count + k) * (size_t)G.m * G.ldx;
   };
-  auto xb_ptr = [&](const GroupPlan& G, int buf, int k) -> __nv_bfloat16* {
+  auto xhi_ptr = [&](const GroupPlan& G, int buf, int k) -> __nv_bfloat16* {
+    return reinterpret_cast<__nv_bfloat16*>(base + G.off_xm) + ((size_t)buf * G.count + k) * (size_t)G.m * G.ldx;
+  };
+  auto xlo_ptr = [&](const GroupPlan& G, int buf, int k) -> __nv_bfloat16* {
     return reinterpret_cast<__nv_bfloat16*>(base + G.off_xb) + ((size_t)buf * G.count + k) * (size_t)G.m * G.ldx;
   };
 
@@ -535,9 +542,15 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
       x.M = d.M;
       x.W = d.W;
       x.O_out = d.O_out;
-      x.xm0 = xm_ptr(G, 0, mp.in_group);
-      x.xb0 = bf16 ? xb_ptr(G, 0, mp.in_group) : nullptr;
-      x.xm_final = xm_ptr(G, final_buf, mp.in_group);
+      if (bf16) {
+        x.xhi0 = xhi_ptr(G, 0, mp.in_group);
+        x.xlo0 = xlo_ptr(G, 0, mp.in_group);
+        x.xhi_final = xhi_ptr(G, final_buf, mp.in_group);
+        x.xlo_final = xlo_ptr(G, final_buf, mp.in_group);
+      } else {
+        x.xm0 = xm_ptr(G, 0, mp.in_group);
+        x.xm_final = xm_ptr(G, final_buf, mp.in_group);
+      }
       x.ldg = d.ldg;
       x.ldm = d.ldm;
       x.ldw = d.ldw;
@@ -622,7 +635,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
             pp->diag_exact = (phase == 1 && it + 2 >= iters) ? 1 : 0;
           }
           if (phase == 0) {          // A = s^2 X X^T
-            pg.opP = bf16 ? (const void*)xb_ptr(G, cur, 0) : (const void*)xm_ptr(G, cur, 0);
+            pg.opP = bf16 ? (const void*)xhi_ptr(G, cur, 0) : (const void*)xm_ptr(G, cur, 0);
             pg.ld_p = G.ldx;
             pg.p_stride = x_stride;
             pg.prev = nullptr;
@@ -643,18 +656,17 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
             pg.opP = Bbuf;
             pg.ld_p = G.lda;
             pg.p_stride = a_stride;
-            pg.opX = bf16 ? (const void*)xb_ptr(G, cur, 0) : (const void*)xm_ptr(G, cur, 0);
+            pg.opX = bf16 ? (const void*)xhi_ptr(G, cur, 0) : (const void*)xm_ptr(G, cur, 0);
             pg.ld_x = G.ldx;
             pg.x_stride = x_stride;
-            pg.prev = xm_ptr(G, cur, 0);
+            // validation mode reads and writes fp32 X directly; the tensor-core
+            // kernel moves the (hi, lo) pair through the tensor maps below
+            pg.prev = bf16 ? nullptr : xm_ptr(G, cur, 0);
             pg.ld_prev = G.ldx;
             pg.prev_stride = x_stride;
-            pg.out = xm_ptr(G, nxt, 0);
+            pg.out = bf16 ? nullptr : xm_ptr(G, nxt, 0);
             pg.ld_out = G.ldx;
             pg.out_stride = x_stride;
-            pg.out_b = (bf16 && it + 1 < iters) ? xb_ptr(G, nxt, 0) : nullptr;
-            pg.ld_outb = G.ldx;
-            pg.outb_stride = x_stride;
           }
           if (bf16) {
             const uint64_t cnt = (uint64_t)G.count;
@@ -665,9 +677,8 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
             CUtensorMap* mb = &pp->map_b[gi - gb];
             CUtensorMap* mc = &pp->map_c[gi - gb];
             CUtensorMap* md = &pp->map_d[gi - gb];
-            const uint64_t xrow32 = (uint64_t)G.ldx * 4, xmat32 = (uint64_t)x_stride * 4;
             if (phase == 0) {
-              ok = encode_map(h, ma, xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 128) &&
+              ok = encode_map(h, ma, xhi_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 128) &&
                    encode_map(h, mc, Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else if (phase == 1) {
@@ -676,10 +687,10 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else {
               ok = encode_map(h, ma, Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
-                   encode_map(h, mb, xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 64) &&
-                   encode_map(h, mc, xm_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow32, xmat32, xmat32 * cnt, 16, 32,
-                              CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
-                   encode_map(h, md, xb_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 16, 32,
+                   encode_map(h, mb, xhi_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 64) &&
+                   encode_map(h, mc, xhi_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 16, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_32B) &&
+                   encode_map(h, md, xlo_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 16, 32,
                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_32B);
             }
             if (!ok) return MUON_ERR_CUDA;

@@ -29,9 +29,15 @@ struct EltMat {
   float* M;
   void* W;
   float* O_out;
-  float* xm0;              // fp32 master copy of X0 (wide orientation), written by K1
-  __nv_bfloat16* xb0;      // bf16 operand copy of X0, or null (fp32 mode)
-  const float* xm_final;   // fp32 X after the last iteration, read by the apply kernel
+  // X0 written by K1 (wide orientation): fp32 (validation mode) or the bf16
+  // pair hi = bf16(x), lo = bf16(x - hi) (tensor-core mode); the other null
+  float* xm0;
+  __nv_bfloat16* xhi0;
+  __nv_bfloat16* xlo0;
+  // X after the last iteration, read by the apply kernel, in the same form
+  const float* xm_final;
+  const __nv_bfloat16* xhi_final;
+  const __nv_bfloat16* xlo_final;
   int64_t ldg, ldm, ldw, ldo, ldx;
   int64_t tile_begin;      // first 64x64 tile of this matrix in the launch-wide numbering
   int64_t partial_begin;   // first partial-sum slot of this matrix

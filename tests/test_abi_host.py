@@ -72,9 +72,9 @@ def _ws(h, items):
 def test_workspace_size_valid(host_handle):
     st, nbytes = _ws(host_handle, [_desc()])
     assert st == B.MUON_OK
-    # two fp32 X buffers, two bf16 X copies, A and B (bf16), plus small headers
+    # X ping-pong as bf16 (hi, lo) pairs, A and B (bf16), plus small headers
     m, n = 256, 512
-    body = 2 * m * n * 4 + 2 * m * n * 2 + 2 * m * m * 2
+    body = 2 * m * n * 2 + 2 * m * n * 2 + 2 * m * m * 2
     assert body <= nbytes <= body + 64 * 1024
 
 
