@@ -275,11 +275,12 @@ def run_gb300(args):
              for i in range(B.MUON_NUM_PHASES)}
     # HBM phases against bandwidth: algorithmic bytes per element
     elems = sum(r * c for r, c in w.shapes)
-    k1_bytes = elems * (4 + 4 + 4 + 4 + 2)       # read G, M; write M, X fp32, X bf16
+    k1_bytes = elems * (4 + 4 + 4 + 2 + 2)       # read G, M; write M, X as bf16 hi + lo
     wbytes = 2 if name != "single_256x512" else 4
-    k5_bytes = elems * (4 + 2 * wbytes)          # read X fp32; read + write W
+    k5_bytes = elems * (4 + 2 * wbytes)          # read X (hi + lo); read + write W
     phase["momentum_norm"]["gbs"] = k1_bytes / (phase["momentum_norm"]["ms_per_step"] / 1e3) / 1e9
-    phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
+    if phase["apply"]["launches_per_step"] > 0:
+        phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
 
     # end to end with the state in pinned host memory: every step copies G,
     # W, M in and W, M out, pipelined in chunks of whole matrices against the

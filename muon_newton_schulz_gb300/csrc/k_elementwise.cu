@@ -108,6 +108,25 @@ __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constan
   if (bt == 0 && threadIdx.x == 0 && p.status) *p.status = 0u;
   const EltMat& e = p.mats[find_mat(p, bt)];
   const int64_t lt = bt - e.tile_begin;
+  if (lt == 0 && p.apply && threadIdx.x < 8) {
+    // publish this matrix's weight-update target for the last GEMM: the W
+    // tensor map (128 B, eight 16-byte pieces) and its descriptor
+    ApplyEntry* ae = p.apply + e.mat;
+    reinterpret_cast<uint4*>(&ae->wmap)[threadIdx.x] = reinterpret_cast<const uint4*>(&e.wmap)[threadIdx.x];
+    if (threadIdx.x == 0) {
+      ApplyDesc a = {};
+      a.W = e.W;
+      a.O_out = e.O_out;
+      a.ldw = e.ldw;
+      a.ldo = e.ldo;
+      a.lr_eff = e.lr_eff;
+      a.w_bf16 = e.w_bf16;
+      a.tall = e.tall;
+      a.rows = e.rows;
+      a.cols = e.cols;
+      ae->d = a;
+    }
+  }
   const int r0 = (int)(lt / e.tiles_c) * kT;
   const int c0 = (int)(lt % e.tiles_c) * kT;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;

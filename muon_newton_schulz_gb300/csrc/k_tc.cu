@@ -504,14 +504,27 @@ __device__ __forceinline__ uint8_t* gemm_out(const EpiCtx& ec, int o) { return e
 // chunk k of this warp covers columns 16 * (slice + k * nslices) of the tile
 __device__ __forceinline__ int gemm_chunk_col(const EpiCtx& ec, int k) { return ec.slice + k * ec.nslices; }
 
+// In the last iteration the output buffers hold the W tile instead (slot b at
+// 4096 + 2048 b), loaded together with the X tile and updated in place.
 __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
                                               EpiCtx& ec, int b, int c0, int r0) {
   if (ec.lane == 0) {
-    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2048);
+    const ApplyEntry* ae = p.apply ? &p.apply[G.first + tl.mat] : nullptr;
+    const uint32_t wbytes = ae ? (ae->d.w_bf16 ? 1024u : 2048u) : 0u;
+    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2048 + wbytes);
     ptx::tma_load_4d(ec.buf + b * 2048, &p.map_c[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
     ptx::tma_load_4d(ec.buf + b * 2048 + 1024, &p.map_d[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
+    if (ae) {
+      if (ae->d.tall) ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, r0, c0, &ec.xfull[b]);
+      else ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, c0, r0, &ec.xfull[b]);
+    }
   }
 }
+
+// W <- W - lr_eff * O on the W tile in slot `ws`, O being this lane's row of
+// X' (16 values).  Wide: 32 rows x 16 columns of W, lane = row.  Tall: W is
+// X transposed, so the tile is 16 rows x 32 columns and lane = column.
+__device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws, int lane, const float (&f)[16]);
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -523,8 +536,76 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
   }
 }
 
+__device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws, int lane, const float (&f)[16]) {
+  const float lr = d.lr_eff;
+  if (!d.tall) {
+    if (d.w_bf16) {   // 32 rows x 16 bf16, 32B swizzle
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint4* q = reinterpret_cast<uint4*>(ws + ptx::sw32_off(lane, i));
+        uint4 u = *q;
+        float wv[8];
+        unpack_bf16x8(u, wv);
+        u.x = pack_bf16x2(fmaf(-lr, f[8 * i + 0], wv[0]), fmaf(-lr, f[8 * i + 1], wv[1]));
+        u.y = pack_bf16x2(fmaf(-lr, f[8 * i + 2], wv[2]), fmaf(-lr, f[8 * i + 3], wv[3]));
+        u.z = pack_bf16x2(fmaf(-lr, f[8 * i + 4], wv[4]), fmaf(-lr, f[8 * i + 5], wv[5]));
+        u.w = pack_bf16x2(fmaf(-lr, f[8 * i + 6], wv[6]), fmaf(-lr, f[8 * i + 7], wv[7]));
+        *q = u;
+      }
+    } else {          // 32 rows x 16 fp32, 64B swizzle
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float4* q = reinterpret_cast<float4*>(ws + ptx::sw64_off(lane, i));
+        float4 v = *q;
+        v.x = fmaf(-lr, f[4 * i + 0], v.x);
+        v.y = fmaf(-lr, f[4 * i + 1], v.y);
+        v.z = fmaf(-lr, f[4 * i + 2], v.z);
+        v.w = fmaf(-lr, f[4 * i + 3], v.w);
+        *q = v;
+      }
+    }
+  } else {
+    if (d.w_bf16) {   // 16 rows x 32 bf16, 64B swizzle: column `lane` of row j
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(ws + ptx::sw64_off(j, lane >> 3) + (lane & 7) * 2);
+        *q = __float2bfloat16_rn(fmaf(-lr, f[j], __bfloat162float(*q)));
+      }
+    } else {          // 16 rows x 32 fp32, 128B swizzle
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float* q = reinterpret_cast<float*>(ws + ptx::sw128_off(j, lane >> 2) + (lane & 3) * 4);
+        *q = fmaf(-lr, f[j], *q);
+      }
+    }
+  }
+}
+
+// Optional fp32 export of O (rows x cols, caller layout) with direct stores.
+__device__ __forceinline__ void gemm_export_o(const ApplyDesc& d, int row, int c0, int m, int n,
+                                              const float (&f)[16]) {
+  if (!d.O_out || row >= m) return;
+  if (!d.tall) {
+    float* o = d.O_out + (int64_t)row * d.ldo + c0;
+    if (c0 + 16 <= n) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(o + 4 * i) = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < n) o[j] = f[j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < n) d.O_out[(int64_t)(c0 + j) * d.ldo + row] = f[j];
+  }
+}
+
 // One 16-column chunk: X' = s * ((a + d) * X + acc), written as the bf16
-// hi/lo pair through the staging buffers.  Returns false on a time-out.
+// hi/lo pair through the staging buffers (or, in the last iteration, applied
+// to W).  Returns false on a time-out.
 __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, EpiCtx& ec,
                                            int col0, int k, int cnt, int r0, float s, float ar,
                                            const uint32_t (&v)[16], volatile int* abort) {
@@ -545,6 +626,27 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
     unpack_bf16x8(*reinterpret_cast<const uint4*>(xl + ptx::sw32_off(lane, i)), lv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) f[8 * i + j] = s * fmaf(ar, hv[j] + lv[j], __uint_as_float(v[8 * i + j]));
+  }
+  if (p.apply) {
+    // last iteration: update the W tile that came with this X tile and store
+    // it; the slot is refilled (chunk k + 2) once the store has read it
+    const ApplyEntry* ae = &p.apply[G.first + tl.mat];
+    uint8_t* ws = gemm_out(ec, b);
+    gemm_apply_slot(ae->d, ws, lane, f);
+    gemm_export_o(ae->d, r0 + lane, c0, G.m, G.n, f);
+    ptx::fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (r0 < G.m) {
+        if (ae->d.tall) ptx::tma_store_2d(&ae->wmap, ws, r0, c0);
+        else ptx::tma_store_2d(&ae->wmap, ws, c0, r0);
+      }
+      ptx::bulk_commit();
+      ptx::bulk_wait_read_all();
+    }
+    __syncwarp();
+    if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * ec.nslices, r0);
+    return true;
   }
   ptx::fence_async_smem();
   if (lane == 0) {
@@ -630,6 +732,8 @@ __device__ __forceinline__ void run_epilogue(const PhaseParams& p, const PairInf
     if (!kGram) {
       const int nch = min(TN / 16, (G.n - col0 + 15) / 16);
       cnt = nch > ec.slice ? (nch - ec.slice + ec.nslices - 1) / ec.nslices : 0;
+      // the W tensor map was written to global memory by the momentum kernel
+      if (p.apply && ec.lane == 0) ptx::fence_tensormap_acquire(&p.apply[G.first + tl.mat].wmap);
       for (int k = 0; k < 2 && k < cnt; ++k) gemm_prefetch(p, G, tl, ec, k, col0 + 16 * gemm_chunk_col(ec, k), r0);
     }
     TC_PROF_T0(t_t);

@@ -33,6 +33,7 @@ constexpr int kMaxProfiledSteps = 1024;
 struct StepEvents {
   std::vector<cudaEvent_t> ev;
   int iters = 0;
+  int apply_launches = 0;
 };
 
 }  // namespace
@@ -72,7 +73,7 @@ struct GroupPlan {
 struct Plan {
   std::vector<MatPlan> mats;
   std::vector<GroupPlan> groups;
-  size_t off_status = 0, off_scale = 0, off_partials = 0, bytes = 0;
+  size_t off_status = 0, off_scale = 0, off_partials = 0, off_apply = 0, bytes = 0;
   int64_t total_partials = 0;
 };
 
@@ -210,7 +211,9 @@ Plan build_plan(const muon_config& cfg, const muon_matrix_desc* d, int n) {
   P.off_scale = off;
   off = align_up(off + P.mats.size() * sizeof(float), 256);
   P.off_partials = off;
-  off = align_up(off + (size_t)partials * sizeof(double), 1024);
+  off = align_up(off + (size_t)partials * sizeof(double), 256);
+  P.off_apply = off;
+  off = align_up(off + P.mats.size() * sizeof(muon::ApplyEntry), 1024);
   for (GroupPlan& G : P.groups) {
     const size_t xel = (size_t)G.count * G.m * G.ldx;
     const size_t ael = (size_t)G.count * G.m * G.lda;
@@ -249,6 +252,30 @@ bool encode_map(muon_handle h, CUtensorMap* map, void* base, uint64_t d0, uint64
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     h->err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+// 2-D map of a caller's weight matrix whose box is one GEMM epilogue chunk:
+// 16 columns x 32 rows (wide), 32 columns x 16 rows (tall: W is X^T), with
+// the swizzle matching the box row (32 B..128 B).
+bool encode_w_map(muon_handle h, CUtensorMap* map, const muon_matrix_desc& d, bool tall) {
+  const bool bf = d.w_dtype == MUON_BF16;
+  const uint64_t es = bf ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)d.cols, (cuuint64_t)d.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(d.ldw * es)};
+  cuuint32_t box[2] = {tall ? 32u : 16u, tall ? 16u : 32u};
+  cuuint32_t estr[2] = {1, 1};
+  const uint64_t row_bytes = box[0] * es;
+  const CUtensorMapSwizzle swz = row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                 : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_128B;
+  CUresult r = h->encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d.W, dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    h->err = "cuTensorMapEncodeTiled (W) failed with CUresult " + std::to_string((int)r);
     return false;
   }
   return true;
@@ -444,7 +471,7 @@ muon_status muon_read_profile(muon_handle h, muon_phase_stats* out) {
     }
     cudaEventElapsedTime(&t, e[e.size() - 2], e[e.size() - 1]);
     out->ms[4] += t;
-    out->launches[4] += 1;
+    out->launches[4] += s.apply_launches;
     out->steps += 1;
   }
   for (StepEvents& s : h->recorded)
@@ -491,6 +518,10 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   uint32_t* status = reinterpret_cast<uint32_t*>(base + P.off_status);
   float* scale = reinterpret_cast<float*>(base + P.off_scale);
   double* partials = reinterpret_cast<double*>(base + P.off_partials);
+  // tensor-core mode applies the weight update in the last GEMM's epilogue,
+  // reading each matrix's W from a table the momentum kernel fills
+  const bool fused_apply = bf16 && iters > 0;
+  muon::ApplyEntry* apply_table = reinterpret_cast<muon::ApplyEntry*>(base + P.off_apply);
 
   StepEvents se;
   auto mark = [&]() {
@@ -532,6 +563,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
     ep.partials = partials;
     ep.scale = scale;
     ep.status = b == 0 ? status : nullptr;
+    ep.apply = fused_apply ? apply_table : nullptr;
     int64_t tiles = 0;
     for (size_t i = b; i < e; ++i) {
       const MatPlan& mp = P.mats[i];
@@ -566,9 +598,11 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
       x.w_bf16 = d.w_dtype == MUON_BF16 ? 1 : 0;
       x.mat = mp.global;
       x.lr_eff = (float)((double)d.lr * (double)cfg.scale_coeff * std::sqrt((double)mp.n));
+      if (fused_apply && !encode_w_map(h, &x.wmap, d, mp.tall)) return false;
       tiles += mp.elt_tiles;
     }
     ep.total_tiles = tiles;
+    return true;
   };
 
   EltParams* ep = new (std::nothrow) EltParams;
@@ -584,7 +618,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   mark();
   for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
     const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
-    fill_elt(*ep, b, e, final_buf);
+    if (!fill_elt(*ep, b, e, final_buf)) return MUON_ERR_CUDA;
     if ((st = launched(muon::launch_momentum_norm(*ep, stream), "momentum/norm kernel")) != MUON_OK) return st;
     if ((st = launched(muon::launch_norm_finalize(*ep, stream), "norm finalize kernel")) != MUON_OK) return st;
   }
@@ -601,6 +635,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
         std::memset(pp, 0, sizeof(*pp));
         pp->ngroups = (int32_t)(ge - gb);
         pp->status = status;
+        pp->apply = (fused_apply && phase == 2 && it + 1 == iters) ? apply_table : nullptr;
         pp->scale = (it == 0 && phase != 1) ? scale : nullptr;
         pp->coef_acc = phase == 1 ? cfg.c : 1.f;
         pp->coef_prev = phase == 1 ? cfg.b : (phase == 2 ? cfg.a : 0.f);
@@ -708,11 +743,14 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
     }
   }
 
-  // ---- apply
-  for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
-    const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
-    fill_elt(*ep, b, e, final_buf);
-    if ((st = launched(muon::launch_apply(*ep, stream), "apply kernel")) != MUON_OK) return st;
+  // ---- apply (a separate kernel unless the last GEMM did it)
+  if (!fused_apply) {
+    for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
+      const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
+      if (!fill_elt(*ep, b, e, final_buf)) return MUON_ERR_CUDA;
+      if ((st = launched(muon::launch_apply(*ep, stream), "apply kernel")) != MUON_OK) return st;
+      se.apply_launches += 1;
+    }
   }
   mark();
   if (!se.ev.empty()) {

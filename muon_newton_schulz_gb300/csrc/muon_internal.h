@@ -13,7 +13,7 @@ struct muon_handle_s;
 namespace muon {
 
 constexpr int kMaxGroups = 16;     // shape groups per Newton-Schulz launch
-constexpr int kMaxEltMats = 128;   // matrices per elementwise launch
+constexpr int kMaxEltMats = 64;    // matrices per elementwise launch
 constexpr int kEltTile = 64;       // elementwise kernels work on 64 x 64 tiles
 constexpr int kSimtTile = 64;      // fp32 validation kernels: 64 x 64 output tiles
 
@@ -22,6 +22,27 @@ constexpr uint32_t kStatusTimeoutProducer = 1u << 0;
 constexpr uint32_t kStatusTimeoutMma = 1u << 1;
 constexpr uint32_t kStatusTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kStatusTimeoutDrain = 1u << 3;
+
+// Weight-update target of one matrix, written into the workspace by the
+// momentum kernel and read by the last GEMM, which applies the update in its
+// epilogue.  wmap is a 2-D tensor map of W whose box covers one epilogue
+// chunk: 16 columns x 32 rows (wide) or 32 columns x 16 rows (tall, where
+// W is X transposed).
+struct ApplyDesc {
+  void* W;
+  float* O_out;
+  int64_t ldw, ldo;
+  float lr_eff;
+  int32_t w_bf16;
+  int32_t tall;
+  int32_t rows, cols;
+  int32_t pad[3];
+};
+
+struct alignas(64) ApplyEntry {
+  CUtensorMap wmap;
+  ApplyDesc d;
+};
 
 // One matrix as the momentum / norm / cast and apply kernels see it.
 struct EltMat {
@@ -48,6 +69,7 @@ struct EltMat {
   int32_t w_bf16;
   int32_t mat;             // global matrix index (scale[])
   float lr_eff;            // lr * scale_coeff * sqrt(max(rows, cols))
+  CUtensorMap wmap;        // W tensor map published for the last GEMM (bf16 mode)
 };
 
 struct EltParams {
@@ -61,6 +83,7 @@ struct EltParams {
   double* partials;        // one sum of squares per 64x64 tile
   float* scale;            // per matrix 1 / (||X0||_F + eps)
   uint32_t* status;        // kernel status word: cleared by the first momentum CTA of a step
+  ApplyEntry* apply;       // per matrix, filled by the momentum kernel (or null)
 };
 
 // One group of same-shape matrices (wide orientation m x n) in one
@@ -99,6 +122,7 @@ struct PhaseParams {
   float coef_prev;         // Gram 2: b (times A); GEMM: a (times X)
   int32_t diag_exact;      // Gram 2: 1 = keep B's diagonal out of the bf16 matrix (fp32 only)
   uint32_t* status;        // kernel status word (bounded waits)
+  const ApplyEntry* apply; // last GEMM: apply W -= lr_eff * X' instead of storing X' (or null)
 };
 
 // Handle accessors for the allocation-free entry point (defined in muon_api.cpp).

@@ -143,10 +143,13 @@ def test_launch_count_and_profile(iters):
     n0 = B.muon_launch_count(ms.h)
     ms.step(Wd, Gd, Md, lrs)
     ms.step(Wd, Gd, Md, lrs)
-    assert B.muon_launch_count(ms.h) - n0 == 2 * (2 + 3 * iters + 1)
+    # tensor-core mode folds the weight update into the last GEMM; with zero
+    # iterations a separate apply kernel runs
+    apply_launches = 0 if iters > 0 else 1
+    assert B.muon_launch_count(ms.h) - n0 == 2 * (2 + 3 * iters + apply_launches)
     st, prof = B.muon_read_profile(ms.h)
     assert st == B.MUON_OK and prof.steps == 2
-    assert prof.launches[0] == 4 and prof.launches[4] == 2
+    assert prof.launches[0] == 4 and prof.launches[4] == 2 * apply_launches
     if iters:
         assert prof.launches[3] == 2 * iters and prof.ms[3] > 0
     ms.close()
