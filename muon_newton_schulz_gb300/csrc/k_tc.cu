@@ -52,7 +52,7 @@
 #define MUON_GRAM_EPI_WARPS 4
 #endif
 #ifndef MUON_GEMM_STAGES
-#define MUON_GEMM_STAGES 4
+#define MUON_GEMM_STAGES (MUON_GEMM_CHUNK == 32 ? 3 : 4)
 #endif
 #ifndef MUON_GEMM_EPI_WARPS
 #define MUON_GEMM_EPI_WARPS 4
@@ -65,7 +65,7 @@
 #define MUON_PAIR_GRAM_STAGES 6
 #endif
 #ifndef MUON_PAIR_GEMM_STAGES
-#define MUON_PAIR_GEMM_STAGES 6
+#define MUON_PAIR_GEMM_STAGES (MUON_GEMM_CHUNK == 32 ? 5 : 6)
 #endif
 #ifndef MUON_PAIR_GRAM_EPI_WARPS
 #define MUON_PAIR_GRAM_EPI_WARPS 4
@@ -104,8 +104,9 @@ struct Cfg {
   static constexpr int kBBytes = kBCols * TK * 2;
   static constexpr int kStageBytes = A_BYTES + kBBytes;
   // Gram: row-major and transposed 32x32 bf16 blocks, double-buffered (8 KiB).
-  // GEMM: two 2 KiB input buffers and two 2 KiB output buffers (hi/lo pairs).
-  static constexpr int kEpiWarpBytes = 8192;
+  // GEMM: two input and two output buffers of (hi, lo) X boxes, 32 rows x
+  // kGemmChunk bf16 each (8 or 16 KiB).
+  static constexpr int kEpiWarpBytes = kGram ? 8192 : 8 * 32 * kGemmChunk * 2;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kBarBytes;
   static_assert(kEpiWarps % 4 == 0, "epilogue warps come in groups of four (one per TMEM lane quarter)");
@@ -496,35 +497,41 @@ __device__ __forceinline__ void gram_tile_epilogue(const PhaseParams& p, const P
 
 // X is kept as a bf16 pair hi = bf16(x), lo = bf16(x - hi) (about 17
 // significant bits); hi is also the MMA operand of the next iteration.
-// Per-warp GEMM staging, each box 32 rows x 16 bf16 (32B swizzle, 1 KiB):
-// input buffer b holds hi at 2048 b and lo at 2048 b + 1024; output buffer o
-// holds hi' at 4096 + 2048 o and lo' at 4096 + 2048 o + 1024.
-__device__ __forceinline__ uint8_t* gemm_out(const EpiCtx& ec, int o) { return ec.buf + 4096 + 2048 * o; }
+// A GEMM epilogue chunk covers 32 rows x kGC columns; each of its X boxes
+// (hi or lo) is 32 rows x kGC bf16 with the swizzle of that row width.
+// Per-warp staging (kXBox = one box): input buffer b holds hi at 2 kXBox b
+// and lo at 2 kXBox b + kXBox; output buffer o holds hi' / lo' at
+// 4 kXBox + 2 kXBox o (+ kXBox).  In the last iteration output slot b holds
+// the W tile loaded with input buffer b (up to 32 x kGC fp32 = 2 kXBox).
+constexpr int kGC = kGemmChunk;
+constexpr int kXBox = 32 * kGC * 2;
+constexpr int kXRowBytes = kGC * 2;
 
-// chunk k of this warp covers columns 16 * (slice + k * nslices) of the tile
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk, int row_bytes) {
+  return row_bytes == 32 ? ptx::sw32_off(row, chunk) : row_bytes == 64 ? ptx::sw64_off(row, chunk)
+                                                                       : ptx::sw128_off(row, chunk);
+}
+
+__device__ __forceinline__ uint8_t* gemm_in(const EpiCtx& ec, int b) { return ec.buf + 2 * kXBox * b; }
+__device__ __forceinline__ uint8_t* gemm_out(const EpiCtx& ec, int o) { return ec.buf + 4 * kXBox + 2 * kXBox * o; }
+
+// chunk k of this warp covers columns kGC * (slice + k * nslices) of the tile
 __device__ __forceinline__ int gemm_chunk_col(const EpiCtx& ec, int k) { return ec.slice + k * ec.nslices; }
 
-// In the last iteration the output buffers hold the W tile instead (slot b at
-// 4096 + 2048 b), loaded together with the X tile and updated in place.
 __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
                                               EpiCtx& ec, int b, int c0, int r0) {
   if (ec.lane == 0) {
     const ApplyEntry* ae = p.apply ? &p.apply[G.first + tl.mat] : nullptr;
-    const uint32_t wbytes = ae ? (ae->d.w_bf16 ? 1024u : 2048u) : 0u;
-    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2048 + wbytes);
-    ptx::tma_load_4d(ec.buf + b * 2048, &p.map_c[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
-    ptx::tma_load_4d(ec.buf + b * 2048 + 1024, &p.map_d[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
+    const uint32_t wbytes = ae ? (ae->d.w_bf16 ? 32u * kGC * 2u : 32u * kGC * 4u) : 0u;
+    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2 * kXBox + wbytes);
+    ptx::tma_load_4d(gemm_in(ec, b), &p.map_c[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
+    ptx::tma_load_4d(gemm_in(ec, b) + kXBox, &p.map_d[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
     if (ae) {
       if (ae->d.tall) ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, r0, c0, &ec.xfull[b]);
       else ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, c0, r0, &ec.xfull[b]);
     }
   }
 }
-
-// W <- W - lr_eff * O on the W tile in slot `ws`, O being this lane's row of
-// X' (16 values).  Wide: 32 rows x 16 columns of W, lane = row.  Tall: W is
-// X transposed, so the tile is 16 rows x 32 columns and lane = column.
-__device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws, int lane, const float (&f)[16]);
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -536,13 +543,16 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
   }
 }
 
-__device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws, int lane, const float (&f)[16]) {
+// W <- W - lr_eff * O on the W tile in slot `ws`, O being this lane's row of
+// X' (kGC values).  Wide: 32 rows x kGC columns of W, lane = row.  Tall: W is
+// X transposed, so the tile is kGC rows x 32 columns and lane = column.
+__device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws, int lane, const float (&f)[kGC]) {
   const float lr = d.lr_eff;
   if (!d.tall) {
-    if (d.w_bf16) {   // 32 rows x 16 bf16, 32B swizzle
+    if (d.w_bf16) {   // rows of kGC bf16
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        uint4* q = reinterpret_cast<uint4*>(ws + ptx::sw32_off(lane, i));
+      for (int i = 0; i < kGC / 8; ++i) {
+        uint4* q = reinterpret_cast<uint4*>(ws + sw_off(lane, i, kGC * 2));
         uint4 u = *q;
         float wv[8];
         unpack_bf16x8(u, wv);
@@ -552,10 +562,10 @@ __device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws,
         u.w = pack_bf16x2(fmaf(-lr, f[8 * i + 6], wv[6]), fmaf(-lr, f[8 * i + 7], wv[7]));
         *q = u;
       }
-    } else {          // 32 rows x 16 fp32, 64B swizzle
+    } else {          // rows of kGC fp32
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float4* q = reinterpret_cast<float4*>(ws + ptx::sw64_off(lane, i));
+      for (int i = 0; i < kGC / 4; ++i) {
+        float4* q = reinterpret_cast<float4*>(ws + sw_off(lane, i, kGC * 4));
         float4 v = *q;
         v.x = fmaf(-lr, f[4 * i + 0], v.x);
         v.y = fmaf(-lr, f[4 * i + 1], v.y);
@@ -565,15 +575,15 @@ __device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws,
       }
     }
   } else {
-    if (d.w_bf16) {   // 16 rows x 32 bf16, 64B swizzle: column `lane` of row j
+    if (d.w_bf16) {   // kGC rows of 32 bf16 (64-byte rows): column `lane` of row j
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kGC; ++j) {
         __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(ws + ptx::sw64_off(j, lane >> 3) + (lane & 7) * 2);
         *q = __float2bfloat16_rn(fmaf(-lr, f[j], __bfloat162float(*q)));
       }
-    } else {          // 16 rows x 32 fp32, 128B swizzle
+    } else {          // kGC rows of 32 fp32 (128-byte rows)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kGC; ++j) {
         float* q = reinterpret_cast<float*>(ws + ptx::sw128_off(j, lane >> 2) + (lane & 3) * 4);
         *q = fmaf(-lr, f[j], *q);
       }
@@ -583,47 +593,47 @@ __device__ __forceinline__ void gemm_apply_slot(const ApplyDesc& d, uint8_t* ws,
 
 // Optional fp32 export of O (rows x cols, caller layout) with direct stores.
 __device__ __forceinline__ void gemm_export_o(const ApplyDesc& d, int row, int c0, int m, int n,
-                                              const float (&f)[16]) {
+                                              const float (&f)[kGC]) {
   if (!d.O_out || row >= m) return;
   if (!d.tall) {
     float* o = d.O_out + (int64_t)row * d.ldo + c0;
-    if (c0 + 16 <= n) {
+    if (c0 + kGC <= n) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < kGC / 4; ++i)
         *reinterpret_cast<float4*>(o + 4 * i) = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
     } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int j = 0; j < kGC; ++j)
         if (c0 + j < n) o[j] = f[j];
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int j = 0; j < kGC; ++j)
       if (c0 + j < n) d.O_out[(int64_t)(c0 + j) * d.ldo + row] = f[j];
   }
 }
 
-// One 16-column chunk: X' = s * ((a + d) * X + acc), written as the bf16
-// hi/lo pair through the staging buffers (or, in the last iteration, applied
-// to W).  Returns false on a time-out.
+// One chunk: X' = s * ((a + d) * X + acc), written as the bf16 hi/lo pair
+// through the staging buffers (or, in the last iteration, applied to W).
+// Returns false on a time-out.
 __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, EpiCtx& ec,
                                            int col0, int k, int cnt, int r0, float s, float ar,
-                                           const uint32_t (&v)[16], volatile int* abort) {
+                                           const uint32_t (&v)[kGC], volatile int* abort) {
   const int lane = ec.lane;
   const int b = k & 1;
-  const int c0 = col0 + 16 * gemm_chunk_col(ec, k);
+  const int c0 = col0 + kGC * gemm_chunk_col(ec, k);
   if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
                               kWaitLimitNs))
     return false;
   ec.xphase ^= 1u << b;
-  const uint8_t* xh = ec.buf + b * 2048;
-  const uint8_t* xl = xh + 1024;
-  float f[16];
+  const uint8_t* xh = gemm_in(ec, b);
+  const uint8_t* xl = xh + kXBox;
+  float f[kGC];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kGC / 8; ++i) {
     float hv[8], lv[8];
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(xh + ptx::sw32_off(lane, i)), hv);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(xl + ptx::sw32_off(lane, i)), lv);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(xh + sw_off(lane, i, kXRowBytes)), hv);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(xl + sw_off(lane, i, kXRowBytes)), lv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) f[8 * i + j] = s * fmaf(ar, hv[j] + lv[j], __uint_as_float(v[8 * i + j]));
   }
@@ -645,21 +655,22 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
       ptx::bulk_wait_read_all();
     }
     __syncwarp();
-    if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * ec.nslices, r0);
+    if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 2 * kGC * ec.nslices, r0);
     return true;
   }
-  ptx::fence_async_smem();
+  // the inputs were consumed above; once every lane is past this point the
+  // input buffer can be refilled
   if (lane == 0) {
     if (ec.out_bufs == 2) ptx::bulk_wait_read_1();
     else ptx::bulk_wait_read_all();
   }
   __syncwarp();
-  if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 32 * ec.nslices, r0);
+  if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 2 * kGC * ec.nslices, r0);
   const int o = ec.out_bufs == 2 ? ec.obuf : 0;
   uint8_t* oh = gemm_out(ec, o);
-  uint8_t* ol = oh + 1024;
+  uint8_t* ol = oh + kXBox;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kGC / 8; ++i) {
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -669,8 +680,8 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
       hw[j] = *reinterpret_cast<const uint32_t*>(&h2);
       lw[j] = *reinterpret_cast<const uint32_t*>(&l2);
     }
-    *reinterpret_cast<uint4*>(oh + ptx::sw32_off(lane, i)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(ol + ptx::sw32_off(lane, i)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    *reinterpret_cast<uint4*>(oh + sw_off(lane, i, kXRowBytes)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(ol + sw_off(lane, i, kXRowBytes)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
   ptx::fence_async_smem();
   __syncwarp();
@@ -683,6 +694,9 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   return true;
 }
 
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&v)[32]) { ptx::tmem_ld_32x32b_x32(taddr, v); }
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&v)[16]) { ptx::tmem_ld_32x32b_x16(taddr, v); }
+
 // The GEMM tile's epilogue for this warp; TMEM loads of chunk k + 1 are in
 // flight while chunk k is processed.
 __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
@@ -693,13 +707,13 @@ __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const P
   // a plus this row's fp32 diagonal term of B (residual or exact diagonal)
   const float ar = p.coef_prev + ((G.diag_in && row < G.m) ? G.diag_in[(int64_t)tl.mat * G.diag_stride + row] : 0.f);
   if (cnt <= 0) return true;
-  uint32_t va[16], vb[16];
-  ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, 0)), va);
+  uint32_t va[kGC], vb[kGC];
+  tmem_ld_chunk(tbase + (uint32_t)(kGC * gemm_chunk_col(ec, 0)), va);
   ptx::tmem_ld_wait_regs(va);
 #pragma unroll 1
   for (int k = 0; k < cnt; k += 2) {
     const bool has1 = k + 1 < cnt;
-    if (has1) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, k + 1)), vb);
+    if (has1) tmem_ld_chunk(tbase + (uint32_t)(kGC * gemm_chunk_col(ec, k + 1)), vb);
     if (!gemm_chunk(p, G, tl, ec, col0, k, cnt, r0, s, ar, va, abort)) {
       if (has1) ptx::tmem_ld_wait_regs(vb);
       return false;
@@ -707,7 +721,7 @@ __device__ __forceinline__ bool gemm_tile_epilogue(const PhaseParams& p, const P
     if (has1) {
       ptx::tmem_ld_wait_regs(vb);
       const bool has2 = k + 2 < cnt;
-      if (has2) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(16 * gemm_chunk_col(ec, k + 2)), va);
+      if (has2) tmem_ld_chunk(tbase + (uint32_t)(kGC * gemm_chunk_col(ec, k + 2)), va);
       const bool okb = gemm_chunk(p, G, tl, ec, col0, k + 1, cnt, r0, s, ar, vb, abort);
       if (has2) ptx::tmem_ld_wait_regs(va);
       if (!okb) return false;
@@ -730,11 +744,11 @@ __device__ __forceinline__ void run_epilogue(const PhaseParams& p, const PairInf
     const int col0 = tl.bj * TN;
     int cnt = 0;
     if (!kGram) {
-      const int nch = min(TN / 16, (G.n - col0 + 15) / 16);
+      const int nch = min(TN / kGC, (G.n - col0 + kGC - 1) / kGC);
       cnt = nch > ec.slice ? (nch - ec.slice + ec.nslices - 1) / ec.nslices : 0;
       // the W tensor map was written to global memory by the momentum kernel
       if (p.apply && ec.lane == 0) ptx::fence_tensormap_acquire(&p.apply[G.first + tl.mat].wmap);
-      for (int k = 0; k < 2 && k < cnt; ++k) gemm_prefetch(p, G, tl, ec, k, col0 + 16 * gemm_chunk_col(ec, k), r0);
+      for (int k = 0; k < 2 && k < cnt; ++k) gemm_prefetch(p, G, tl, ec, k, col0 + kGC * gemm_chunk_col(ec, k), r0);
     }
     TC_PROF_T0(t_t);
     if (!wait_role<false>(&tfull[acc], acc_phase, abort, p.status, kStatusTimeoutEpilogue)) ok = false;

@@ -265,7 +265,8 @@ bool encode_w_map(muon_handle h, CUtensorMap* map, const muon_matrix_desc& d, bo
   const uint64_t es = bf ? 2 : 4;
   cuuint64_t dims[2] = {(cuuint64_t)d.cols, (cuuint64_t)d.rows};
   cuuint64_t strides[1] = {(cuuint64_t)(d.ldw * es)};
-  cuuint32_t box[2] = {tall ? 32u : 16u, tall ? 16u : 32u};
+  const cuuint32_t chunk = (cuuint32_t)muon::kGemmChunk;
+  cuuint32_t box[2] = {tall ? 32u : chunk, tall ? chunk : 32u};
   cuuint32_t estr[2] = {1, 1};
   const uint64_t row_bytes = box[0] * es;
   const CUtensorMapSwizzle swz = row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
@@ -721,12 +722,15 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
                    encode_map(h, mc, Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else {
+              // epilogue boxes: 32 rows x kGemmChunk bf16 (32- or 64-byte rows)
+              const uint32_t gc = (uint32_t)muon::kGemmChunk;
+              const CUtensorMapSwizzle eswz = gc == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
               ok = encode_map(h, ma, Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
                    encode_map(h, mb, xhi_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 64, 64) &&
-                   encode_map(h, mc, xhi_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 16, 32,
-                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_32B) &&
-                   encode_map(h, md, xlo_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, 16, 32,
-                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_32B);
+                   encode_map(h, mc, xhi_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, gc, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, eswz) &&
+                   encode_map(h, md, xlo_ptr(G, 0, 0), G.n, G.m, cnt, 2, xrow, xmat, xmat * cnt, gc, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, eswz);
             }
             if (!ok) return MUON_ERR_CUDA;
           }

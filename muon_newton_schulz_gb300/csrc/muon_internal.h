@@ -148,6 +148,14 @@ constexpr int kTcM = 128;
 constexpr int kTcN = 256;
 constexpr int kTcK = 64;
 
+// Columns per GEMM epilogue chunk (16 or 32): the X tiles it moves are
+// 32 rows x chunk bf16, i.e. 32- or 64-byte rows.
+#ifndef MUON_GEMM_CHUNK
+#define MUON_GEMM_CHUNK 32
+#endif
+constexpr int kGemmChunk = MUON_GEMM_CHUNK;
+static_assert(kGemmChunk == 16 || kGemmChunk == 32, "GEMM epilogue chunk of 16 or 32 columns");
+
 // The Newton-Schulz phases run on CTA pairs (256 x 256 tiles) unless built
 // with -DMUON_USE_PAIR=0 (single CTAs, 128 x 256 tiles).
 #ifndef MUON_USE_PAIR
