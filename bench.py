@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--e2e-chunk", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step in a CUDA graph and time its replays (no per-phase profile)")
     return ap.parse_args()
 
 
@@ -208,7 +210,10 @@ def run_gb300(args):
     mode = B.MUON_MODE_BF16 if args.mode == "bf16" else B.MUON_MODE_FP32_VALIDATE
 
     B.load_library(build_if_missing=True)
-    # every rank owns whole matrices (its own replica of the workload)
+    # every rank owns whole matrices: its own set, shaped like the workload
+    # (another layer's experts), seeded by rank
+    if rank:
+        w = wl.Workload(w.name, w.specs, lr=w.lr, seed_base=w.seed_base + 100000 * rank)
     Ws, Gs, Ms, lrs = wl.make_workload(w, dev, steady_momentum=True)
     ms = B.MuonStep(local, mode=mode)
     descs, n = ms.descs_from_tensors(Ws, Gs, Ms, lrs)
@@ -232,8 +237,23 @@ def run_gb300(args):
             import torch.distributed as dist
             dist.barrier()
 
-    B.muon_set_profiling(ms.h, True)
-    B.muon_read_profile(ms.h)  # clear
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        n_before = B.muon_launch_count(ms.h)
+        with torch.cuda.graph(graph, stream=side):
+            st = B.muon_step(ms.h, descs, n, ws.data_ptr(), ws.numel(), side.cuda_stream)
+            if st != B.MUON_OK:
+                raise B.MuonError(st, B.muon_last_error_message(ms.h))
+        launches_per_step = B.muon_launch_count(ms.h) - n_before
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+    else:
+        B.muon_set_profiling(ms.h, True)
+        B.muon_read_profile(ms.h)  # clear
     n_launch0 = B.muon_launch_count(ms.h)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -242,11 +262,14 @@ def run_gb300(args):
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-    launches = B.muon_launch_count(ms.h) - n_launch0
+    launches = B.muon_launch_count(ms.h) - n_launch0 if graph is None else launches_per_step * args.steps
     ms_total = e0.elapsed_time(e1)
     st, prof = B.muon_read_profile(ms.h)
     B.muon_set_profiling(ms.h, False)
@@ -266,21 +289,24 @@ def run_gb300(args):
     peak_tf, hbm_gbs, peak_kind = peaks()
 
     # dominant kernel: the GEMM with the a X epilogue (61% of the flops)
-    gemm_ms = prof.ms[3] / max(1, prof.launches[3])
     gemm_flops = sum(2.0 * min(r, c) ** 2 * max(r, c) for r, c in w.shapes)
-    achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
     traffic = measured_traffic(name)
-    phase = {B.PHASE_NAMES[i]: {"ms_per_step": prof.ms[i] / max(1, prof.steps),
-                                "launches_per_step": prof.launches[i] / max(1, prof.steps)}
-             for i in range(B.MUON_NUM_PHASES)}
-    # HBM phases against bandwidth: algorithmic bytes per element
-    elems = sum(r * c for r, c in w.shapes)
-    k1_bytes = elems * (4 + 4 + 4 + 2 + 2)       # read G, M; write M, X as bf16 hi + lo
-    wbytes = 2 if name != "single_256x512" else 4
-    k5_bytes = elems * (4 + 2 * wbytes)          # read X (hi + lo); read + write W
-    phase["momentum_norm"]["gbs"] = k1_bytes / (phase["momentum_norm"]["ms_per_step"] / 1e3) / 1e9
-    if phase["apply"]["launches_per_step"] > 0:
-        phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
+    phase = None
+    gemm_ms = achieved = None
+    if prof.steps > 0:   # per-phase events (not recorded inside a CUDA graph)
+        gemm_ms = prof.ms[3] / max(1, prof.launches[3])
+        achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
+        phase = {B.PHASE_NAMES[i]: {"ms_per_step": prof.ms[i] / max(1, prof.steps),
+                                    "launches_per_step": prof.launches[i] / max(1, prof.steps)}
+                 for i in range(B.MUON_NUM_PHASES)}
+        # HBM phases against bandwidth: algorithmic bytes per element
+        elems = sum(r * c for r, c in w.shapes)
+        k1_bytes = elems * (4 + 4 + 4 + 2 + 2)       # read G, M; write M, X as bf16 hi + lo
+        wbytes = 2 if name != "single_256x512" else 4
+        k5_bytes = elems * (4 + 2 * wbytes)          # read X (hi + lo); read + write W
+        phase["momentum_norm"]["gbs"] = k1_bytes / (phase["momentum_norm"]["ms_per_step"] / 1e3) / 1e9
+        if phase["apply"]["launches_per_step"] > 0:
+            phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
 
     # end to end with the state in pinned host memory: every step copies G,
     # W, M in and W, M out, pipelined in chunks of whole matrices against the
@@ -329,9 +355,9 @@ def run_gb300(args):
         "tflops_symmetric": sym_flops / (ms_step / 1e3) / 1e12 * world,
         "tflops_dense_equivalent": dense_flops / (ms_step / 1e3) / 1e12 * world,
         "frac_of_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / peak_tf,
-        "roofline": {"kernel": "k_ns_tc<GEMM> (gemm_update)", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "k_ns_tc_pair<GEMM> (gemm_update)", "bound": "tensor", "achieved": achieved,
                      "peak": peak_tf, "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": traffic,
+                     "frac": achieved / peak_tf if achieved is not None else None, "traffic": traffic,
                      "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": gemm_ms},
         "phases": phase,
         "e2e": e2e,

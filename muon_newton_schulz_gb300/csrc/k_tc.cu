@@ -211,7 +211,10 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, const PairInf
       uint8_t* sa = smem + stage * C::kStageBytes;
       uint8_t* sb = sa + A_BYTES;
       const int k0 = kb * TK;
-      if (!kPair || pi.rank == 0) {
+      if (p.withhold_loads) {
+        // failure-path test: nothing arrives on the stage barriers, so the
+        // MMA's bounded wait runs out and the kernel reports a time-out
+      } else if (!kPair || pi.rank == 0) {
         // the even CTA's barrier counts the bytes of both CTAs of a pair
         ptx::mbar_arrive_expect_tx(&full[stage], (kPair ? 2 : 1) * C::kStageBytes);
         if (kGram) {
@@ -239,7 +242,7 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, const PairInf
             ptx::tma_load_4d_pair(sb + q * (64 * TK * 2), mb, bcol + 64 * q, k0, tl.mat, G.buf_in, bar);
         }
       }
-      outstanding |= 1u << stage;
+      if (!p.withhold_loads) outstanding |= 1u << stage;
       fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == S) { stage = 0; phase ^= 1u; }
     }

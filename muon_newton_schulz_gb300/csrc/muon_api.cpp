@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <new>
@@ -522,6 +523,8 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   // tensor-core mode applies the weight update in the last GEMM's epilogue,
   // reading each matrix's W from a table the momentum kernel fills
   const bool fused_apply = bf16 && iters > 0;
+  const char* withhold_env = std::getenv("MUON_GB300_TEST_WITHHOLD_LOADS");
+  const bool withhold = bf16 && withhold_env && withhold_env[0] == '1';
   muon::ApplyEntry* apply_table = reinterpret_cast<muon::ApplyEntry*>(base + P.off_apply);
 
   StepEvents se;
@@ -637,6 +640,9 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
         pp->ngroups = (int32_t)(ge - gb);
         pp->status = status;
         pp->apply = (fused_apply && phase == 2 && it + 1 == iters) ? apply_table : nullptr;
+        // failure-path test hook (environment, read per step): the step's
+        // first Gram launch withholds its loads so its bounded waits expire
+        pp->withhold_loads = (withhold && it == 0 && phase == 0 && gb == 0) ? 1 : 0;
         pp->scale = (it == 0 && phase != 1) ? scale : nullptr;
         pp->coef_acc = phase == 1 ? cfg.c : 1.f;
         pp->coef_prev = phase == 1 ? cfg.b : (phase == 2 ? cfg.a : 0.f);

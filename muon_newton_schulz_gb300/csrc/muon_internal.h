@@ -123,6 +123,7 @@ struct PhaseParams {
   int32_t diag_exact;      // Gram 2: 1 = keep B's diagonal out of the bf16 matrix (fp32 only)
   uint32_t* status;        // kernel status word (bounded waits)
   const ApplyEntry* apply; // last GEMM: apply W -= lr_eff * X' instead of storing X' (or null)
+  int32_t withhold_loads;  // test hook: the producer issues no loads, so the waits run out
 };
 
 // Handle accessors for the allocation-free entry point (defined in muon_api.cpp).

@@ -67,6 +67,13 @@ WORKLOADS = {
         MatrixSpec(6144, 6144, 4, "svd", log10_lo=-5.0),
         MatrixSpec(2048, 6144, 8, "svd", log10_lo=-5.0),
     ), seed_base=5000),
+    # the pages' other GEMM shapes: the MLP expansion 3072 x 12288
+    # (hotelren.com/news/3048137, section 2.1) and the Q projection weight
+    # 2048 x 1024 (jsqmd.com/news/1098463, section 3.1)
+    "mlp_and_qproj": Workload("mlp_and_qproj", (
+        MatrixSpec(3072, 12288, 1, "gauss", 1e-3),
+        MatrixSpec(2048, 1024, 4, "gauss", 1e-3),
+    ), seed_base=6000),
     # four experts of the same shape: a profiling case that still exceeds L2
     "experts_4x2048x8192": Workload("experts_4x2048x8192", (MatrixSpec(2048, 8192, 4, "gauss", 1e-3),), seed_base=2000),
     # scaled-down versions with the same structure, used by parity tests

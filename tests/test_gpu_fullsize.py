@@ -70,3 +70,8 @@ def test_single_256x512_full():
 
 def test_experts_128x2048x8192_sampled():
     _check_samples("experts_128x2048x8192", {0, 127})
+
+
+def test_mlp_and_qproj_shapes():
+    # 3072 x 12288 (wide) and 2048 x 1024 (tall) in one ragged batch
+    _check_samples("mlp_and_qproj", {0, 1, 4})
