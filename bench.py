@@ -34,7 +34,7 @@ KERNEL_SOURCES = ["muon_newton_schulz_gb300/csrc/k_tc.cu", "muon_newton_schulz_g
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=None)
@@ -88,29 +88,44 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock, power and throttle reasons, each with its
+    own timestamp, so that the summary covers the timed window only."""
 
-    def __init__(self, index: int):
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int, period_ms: int = 25):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.window = None
 
-    def __enter__(self):
+    def start(self):
+        """Starts sampling and waits (up to 5 s) until the first sample is written."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index),
-                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
         return self
 
-    def __exit__(self, *a):
+    def mark(self, t_begin: float, t_end: float):
+        self.window = (t_begin, t_end)
+
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -118,6 +133,16 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.fh.close()
+            self.proc = None
+
+    @staticmethod
+    def _epoch(ts: str):
+        ts = ts.strip()
+        frac = 0.0
+        if "." in ts:
+            ts, f = ts.split(".", 1)
+            frac = float("0." + f)
+        return time.mktime(time.strptime(ts, "%Y/%m/%d %H:%M:%S")) + frac
 
     def summary(self):
         out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
@@ -125,23 +150,27 @@ class ClockSampler:
             rows = [l.strip().split(", ") for l in open(self.path) if l.strip()]
         except Exception:
             return out
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
         for r in rows:
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
+                parsed.append((self._epoch(r[0]), float(r[2]), float(r[3]), float(r[4]),
+                               [r[6 + k].strip().lower() == "active" for k in range(4)]))
             except ValueError:
                 continue
-            for k, name in enumerate(names):
-                if r[5 + k].strip().lower() == "active":
-                    reasons.add(name)
-        if sm:
-            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                   "samples": len(sm)}
-        return out
+        if not parsed:
+            return out
+        sel = parsed
+        if self.window is not None:
+            b, e = self.window
+            sel = [x for x in parsed if b <= x[0] <= e]
+            if not sel:   # window shorter than the sampling period: nearest samples
+                sel = sorted(parsed, key=lambda x: min(abs(x[0] - b), abs(x[0] - e)))[:2]
+        reasons = sorted({self.REASONS[k] for x in sel for k in range(4) if x[4][k]})
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_min_mhz": min(x[1] for x in sel),
+                "sm_max_mhz": max(x[2] for x in sel), "power_w_median": statistics.median(x[3] for x in sel),
+                "reasons": reasons, "samples": len(sel), "period_ms": self.period_ms}
 
 
 def oracle_baseline(workload, n_matrices: int, steps: int, warmup: int):
@@ -226,10 +255,12 @@ def run_gb300(args):
         if st != B.MUON_OK:
             raise B.MuonError(st, B.muon_last_error_message(ms.h))
 
+    clk = ClockSampler(local).start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if ms.check_status() != B.MUON_OK:
+        clk.stop()
         raise RuntimeError("kernel status not OK after warm-up: " + B.muon_last_error_message(ms.h))
 
     def barrier():
@@ -257,18 +288,22 @@ def run_gb300(args):
     n_launch0 = B.muon_launch_count(ms.h)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
-                step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_begin = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    barrier()
+    time.sleep(2 * clk.period_ms / 1e3)   # let the last samples of the window land
+    clk.mark(t_begin, t_end)
+    clk.stop()
     launches = B.muon_launch_count(ms.h) - n_launch0 if graph is None else launches_per_step * args.steps
     ms_total = e0.elapsed_time(e1)
     st, prof = B.muon_read_profile(ms.h)
