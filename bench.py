@@ -28,7 +28,7 @@ METRIC = "Muon NS-orthogonalised matrices/sec and TFLOP/s (5 iters) vs GB300 BF1
 UNIT = "matrices/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCES = ["muon_newton_schulz_gb300/csrc/k_tc.cu", "muon_newton_schulz_gb300/csrc/ptx_sm100.cuh",
-                  "muon_newton_schulz_gb300/csrc/muon_internal.h"]
+                  "muon_newton_schulz_gb300/csrc/muon_internal.h", "muon_newton_schulz_gb300/csrc/launch_util.cuh"]
 
 
 def parse():

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "muon_internal.h"
+#include "launch_util.cuh"
 
 namespace muon {
 
@@ -103,6 +104,8 @@ __device__ __forceinline__ void load_x4(const EltMat& e, int64_t off, float (&v)
 __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constant__ EltParams p) {
   __shared__ float tile[kT][kT + 1];
   __shared__ double red[kThreads / 32];
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int64_t bt = block_tile();
   if (bt >= p.total_tiles) return;
   if (bt == 0 && threadIdx.x == 0 && p.status) *p.status = 0u;
@@ -199,6 +202,8 @@ __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constan
 // scale = 1 / (sqrt(sum) + eps).
 __global__ void __launch_bounds__(kThreads) k_norm_finalize(const __grid_constant__ EltParams p) {
   __shared__ double red[kThreads / 32];
+  grid_dependency_wait();
+  allow_dependent_launch();
   const EltMat& e = p.mats[blockIdx.x];
   double s = 0.0;
   for (int64_t i = threadIdx.x; i < e.ntiles; i += kThreads) s += p.partials[e.partial_begin + i];
@@ -210,6 +215,8 @@ __global__ void __launch_bounds__(kThreads) k_norm_finalize(const __grid_constan
 // W <- W - lr_eff * O, O = X_final (wide) oriented back to rows x cols.
 __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ EltParams p) {
   __shared__ float tile[kT][kT + 1];
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int64_t bt = block_tile();
   if (bt >= p.total_tiles) return;
   const EltMat& e = p.mats[find_mat(p, bt)];
@@ -306,22 +313,19 @@ dim3 tile_grid(int64_t tiles) {
 
 }  // namespace
 
-int launch_momentum_norm(const EltParams& p, void* stream) {
+int launch_momentum_norm(const EltParams& p, void* stream, bool pdl) {
   if (p.total_tiles == 0) return 0;
-  k_momentum_norm<<<tile_grid(p.total_tiles), kThreads, 0, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_momentum_norm, tile_grid(p.total_tiles), dim3(kThreads), 0, stream, pdl, p);
 }
 
-int launch_norm_finalize(const EltParams& p, void* stream) {
+int launch_norm_finalize(const EltParams& p, void* stream, bool pdl) {
   if (p.nmats == 0) return 0;
-  k_norm_finalize<<<p.nmats, kThreads, 0, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_norm_finalize, dim3((unsigned)p.nmats), dim3(kThreads), 0, stream, pdl, p);
 }
 
-int launch_apply(const EltParams& p, void* stream) {
+int launch_apply(const EltParams& p, void* stream, bool pdl) {
   if (p.total_tiles == 0) return 0;
-  k_apply<<<tile_grid(p.total_tiles), kThreads, 0, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_apply, tile_grid(p.total_tiles), dim3(kThreads), 0, stream, pdl, p);
 }
 
 }  // namespace muon

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "muon_internal.h"
+#include "launch_util.cuh"
 
 namespace muon {
 
@@ -45,6 +46,8 @@ __device__ __forceinline__ Tile decode(const PhaseParams& p, int t, bool gram) {
 __global__ void __launch_bounds__(kThreads) k_gram_f32(const __grid_constant__ PhaseParams p) {
   __shared__ float As[KC][T + 4];
   __shared__ float Bs[KC][T + 4];
+  grid_dependency_wait();
+  allow_dependent_launch();
   const Tile tl = decode(p, blockIdx.x, true);
   const PhaseGroup& G = p.g[tl.g];
   const float* P = reinterpret_cast<const float*>(G.opP) + (int64_t)tl.mat * G.p_stride;
@@ -101,6 +104,8 @@ __global__ void __launch_bounds__(kThreads) k_gram_f32(const __grid_constant__ P
 __global__ void __launch_bounds__(kThreads) k_gemm_f32(const __grid_constant__ PhaseParams p) {
   __shared__ float As[KC][T + 4];
   __shared__ float Bs[KC][T + 4];
+  grid_dependency_wait();
+  allow_dependent_launch();
   const Tile tl = decode(p, blockIdx.x, false);
   const PhaseGroup& G = p.g[tl.g];
   const float* Bm = reinterpret_cast<const float*>(G.opP) + (int64_t)tl.mat * G.p_stride;
@@ -160,16 +165,14 @@ __global__ void __launch_bounds__(kThreads) k_gemm_f32(const __grid_constant__ P
 
 }  // namespace
 
-int launch_gram_f32(const PhaseParams& p, void* stream) {
+int launch_gram_f32(const PhaseParams& p, void* stream, bool pdl) {
   if (p.total_tiles == 0) return 0;
-  k_gram_f32<<<p.total_tiles, kThreads, 0, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_gram_f32, dim3((unsigned)p.total_tiles), dim3(kThreads), 0, stream, pdl, p);
 }
 
-int launch_gemm_f32(const PhaseParams& p, void* stream) {
+int launch_gemm_f32(const PhaseParams& p, void* stream, bool pdl) {
   if (p.total_tiles == 0) return 0;
-  k_gemm_f32<<<p.total_tiles, kThreads, 0, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_gemm_f32, dim3((unsigned)p.total_tiles), dim3(kThreads), 0, stream, pdl, p);
 }
 
 }  // namespace muon

@@ -41,6 +41,7 @@
 
 #include "muon_internal.h"
 #include "ptx_sm100.cuh"
+#include "launch_util.cuh"
 
 // Pipeline shape of the single-CTA instantiations (ring stages, epilogue
 // warps, output staging buffers of the GEMM epilogue).  Defaults are the
@@ -120,11 +121,13 @@ struct Tile { int g, mat, bi, bj; };
 // over CTAs into 64-bit slots after the status word, read from the workspace.
 //   [1] MMA waiting for a full stage   [2] MMA waiting for a free accumulator
 //   [3] TMA waiting for an empty stage [4] epilogue waiting for an accumulator
-//   [5] CTA lifetime; slots 6-10 the same for the GEMM instantiation
+//   [5] CTA lifetime; slots 6-10 the same for the GEMM, 11-15 for the Gram
+//   launches that combine with the previous A (Gram 2)
 #ifdef MUON_TC_PROFILE
 #define TC_PROF_T0(v) const long long v = clock64()
-#define TC_PROF_ADD(slot, v) atomicAdd(reinterpret_cast<unsigned long long*>(p.status) + (slot) + (kGram ? 0 : 5), \
-                                       (unsigned long long)(clock64() - (v)))
+#define TC_PROF_ADD(slot, v)                                                                          \
+  atomicAdd(reinterpret_cast<unsigned long long*>(p.status) + (slot) + (kGram ? (p.g[0].prev ? 10 : 0) : 5), \
+            (unsigned long long)(clock64() - (v)))
 #else
 #define TC_PROF_T0(v)
 #define TC_PROF_ADD(slot, v)
@@ -853,6 +856,10 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
   else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up done: from here on this CTA reads and writes what earlier kernels
+  // of the step produced
+  grid_dependency_wait();
+  if (threadIdx.x == 0) allow_dependent_launch();
 
   if (warp == 0) {
     if (lane == 0) run_producer<kGram, kPair>(p, pi, smem, full, empty, abort);
@@ -901,20 +908,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kGram, true>::kT
 }
 
 template <bool kGram>
-int launch_tc(const PhaseParams& p, int grid, void* stream) {
+int launch_tc(const PhaseParams& p, int grid, void* stream, bool pdl) {
   using C = Cfg<kGram, false>;
   if (p.total_tiles == 0) return 0;
   cudaError_t e = cudaFuncSetAttribute(k_ns_tc<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   if (grid > p.total_tiles) grid = p.total_tiles;
-  k_ns_tc<kGram><<<grid, C::kThreads, C::kSmemBytes, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_ns_tc<kGram>, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, stream, pdl, p);
 }
 
 // Pairs: as many co-resident clusters of two as the device holds, capped by
 // the number of tiles.
 template <bool kGram>
-int launch_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
+int launch_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool pdl) {
   using C = Cfg<kGram, true>;
   if (p.total_tiles == 0) return 0;
   cudaError_t e =
@@ -935,20 +941,24 @@ int launch_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
   fprintf(stderr, "k_ns_tc_pair<%d>: %d clusters of 2 for %d tiles (%d SMs)\n", (int)kGram, clusters, p.total_tiles,
           sm_count);
 #endif
-  k_ns_tc_pair<kGram><<<2 * clusters, C::kThreads, C::kSmemBytes, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  return launch_kernel(k_ns_tc_pair<kGram>, dim3((unsigned)(2 * clusters)), dim3(C::kThreads), C::kSmemBytes, stream,
+                       pdl, p);
 }
 
 }  // namespace
 
 int tc_smem_bytes() { return Cfg<true, false>::kSmemBytes; }
-int launch_gram_tc(const PhaseParams& p, int grid, void* stream) { return launch_tc<true>(p, grid, stream); }
-int launch_gemm_tc(const PhaseParams& p, int grid, void* stream) { return launch_tc<false>(p, grid, stream); }
-int launch_gram_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
-  return launch_tc_pair<true>(p, sm_count, stream);
+int launch_gram_tc(const PhaseParams& p, int grid, void* stream, bool pdl) {
+  return launch_tc<true>(p, grid, stream, pdl);
 }
-int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream) {
-  return launch_tc_pair<false>(p, sm_count, stream);
+int launch_gemm_tc(const PhaseParams& p, int grid, void* stream, bool pdl) {
+  return launch_tc<false>(p, grid, stream, pdl);
+}
+int launch_gram_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool pdl) {
+  return launch_tc_pair<true>(p, sm_count, stream, pdl);
+}
+int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool pdl) {
+  return launch_tc_pair<false>(p, sm_count, stream, pdl);
 }
 
 }  // namespace muon

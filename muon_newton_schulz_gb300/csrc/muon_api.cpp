@@ -619,12 +619,16 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   struct Free { EltParams* a; PhaseParams* b; ~Free() { delete a; delete b; } } free_guard{ep, pp};
 
   const int final_buf = iters % 2;
+  // every launch after the step's first is a programmatic dependent of the
+  // kernel before it (the kernels wait for their predecessor themselves)
+  bool pdl = false;
   mark();
   for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
     const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
     if (!fill_elt(*ep, b, e, final_buf)) return MUON_ERR_CUDA;
-    if ((st = launched(muon::launch_momentum_norm(*ep, stream), "momentum/norm kernel")) != MUON_OK) return st;
-    if ((st = launched(muon::launch_norm_finalize(*ep, stream), "norm finalize kernel")) != MUON_OK) return st;
+    if ((st = launched(muon::launch_momentum_norm(*ep, stream, pdl), "momentum/norm kernel")) != MUON_OK) return st;
+    pdl = muon::kUsePdl;
+    if ((st = launched(muon::launch_norm_finalize(*ep, stream, pdl), "norm finalize kernel")) != MUON_OK) return st;
   }
   mark();
 
@@ -744,9 +748,11 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
         pp->total_tiles = tiles;
         int rc;
         if (bf16 && muon::kUsePair)
-          rc = gram ? muon::launch_gram_tc_pair(*pp, h->sm_count, stream) : muon::launch_gemm_tc_pair(*pp, h->sm_count, stream);
-        else if (bf16) rc = gram ? muon::launch_gram_tc(*pp, grid, stream) : muon::launch_gemm_tc(*pp, grid, stream);
-        else rc = gram ? muon::launch_gram_f32(*pp, stream) : muon::launch_gemm_f32(*pp, stream);
+          rc = gram ? muon::launch_gram_tc_pair(*pp, h->sm_count, stream, pdl)
+                    : muon::launch_gemm_tc_pair(*pp, h->sm_count, stream, pdl);
+        else if (bf16)
+          rc = gram ? muon::launch_gram_tc(*pp, grid, stream, pdl) : muon::launch_gemm_tc(*pp, grid, stream, pdl);
+        else rc = gram ? muon::launch_gram_f32(*pp, stream, pdl) : muon::launch_gemm_f32(*pp, stream, pdl);
         if ((st = launched(rc, gram ? "Gram kernel" : "GEMM kernel")) != MUON_OK) return st;
       }
       mark();
@@ -758,7 +764,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
     for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
       const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
       if (!fill_elt(*ep, b, e, final_buf)) return MUON_ERR_CUDA;
-      if ((st = launched(muon::launch_apply(*ep, stream), "apply kernel")) != MUON_OK) return st;
+      if ((st = launched(muon::launch_apply(*ep, stream, pdl), "apply kernel")) != MUON_OK) return st;
       se.apply_launches += 1;
     }
   }

@@ -26,8 +26,8 @@ constexpr uint32_t kStatusTimeoutDrain = 1u << 3;
 // Weight-update target of one matrix, written into the workspace by the
 // momentum kernel and read by the last GEMM, which applies the update in its
 // epilogue.  wmap is a 2-D tensor map of W whose box covers one epilogue
-// chunk: 16 columns x 32 rows (wide) or 32 columns x 16 rows (tall, where
-// W is X transposed).
+// chunk: kGemmChunk columns x 32 rows (wide) or 32 columns x kGemmChunk rows
+// (tall, where W is X transposed).
 struct ApplyDesc {
   void* W;
   float* O_out;
@@ -39,7 +39,7 @@ struct ApplyDesc {
   int32_t pad[3];
 };
 
-struct alignas(64) ApplyEntry {
+struct ApplyEntry {   // 128-byte aligned through CUtensorMap
   CUtensorMap wmap;
   ApplyDesc d;
 };
@@ -102,9 +102,9 @@ struct PhaseGroup {
   const void* opP; int64_t ld_p; int64_t p_stride;   // Gram operand / GEMM left operand
   const void* opX; int64_t ld_x; int64_t x_stride;   // GEMM right operand
   // epilogue
-  const void* prev; int64_t ld_prev; int64_t prev_stride;  // Gram 2: A; GEMM: X (fp32 master)
-  void* out; int64_t ld_out; int64_t out_stride;           // Gram: A or B; GEMM: X' (fp32)
-  __nv_bfloat16* out_b; int64_t ld_outb; int64_t outb_stride;  // GEMM: bf16 X' or null
+  const void* prev; int64_t ld_prev; int64_t prev_stride;  // Gram 2: A; GEMM (validation mode): fp32 X
+  void* out; int64_t ld_out; int64_t out_stride;           // Gram: A or B; GEMM (validation mode): fp32 X'
+  __nv_bfloat16* out_b; int64_t ld_outb; int64_t outb_stride;  // unused (null)
   // fp32 per-row diagonal terms (tensor-core path; null elsewhere), stride per matrix
   const float* diag_in; float* diag_out; int64_t diag_stride;
 };
@@ -112,8 +112,8 @@ struct PhaseGroup {
 struct PhaseParams {
   CUtensorMap map_a[kMaxGroups];   // tensor-core path: left operand (and Gram right operand)
   CUtensorMap map_b[kMaxGroups];   // tensor-core path: GEMM right operand (MN-major X)
-  CUtensorMap map_c[kMaxGroups];   // epilogue: Gram output (bf16, 32x32 box) / GEMM fp32 X in+out (16x32 box)
-  CUtensorMap map_d[kMaxGroups];   // epilogue: GEMM bf16 X out (16x32 box)
+  CUtensorMap map_c[kMaxGroups];   // epilogue: Gram output (bf16, 32x32 box) / GEMM X hi in+out (32 rows x chunk)
+  CUtensorMap map_d[kMaxGroups];   // epilogue: GEMM X lo in+out (32 rows x chunk)
   PhaseGroup g[kMaxGroups];
   int32_t ngroups;
   int32_t total_tiles;
@@ -131,16 +131,24 @@ int handle_device(::muon_handle_s* h);
 void set_handle_error(::muon_handle_s* h, const std::string& msg);
 
 // Launch wrappers (defined in the .cu files).  Each returns the launch's
-// cudaError_t as int.
-int launch_momentum_norm(const EltParams& p, void* stream);
-int launch_norm_finalize(const EltParams& p, void* stream);
-int launch_apply(const EltParams& p, void* stream);
-int launch_gram_f32(const PhaseParams& p, void* stream);
-int launch_gemm_f32(const PhaseParams& p, void* stream);
-int launch_gram_tc(const PhaseParams& p, int grid, void* stream);
-int launch_gemm_tc(const PhaseParams& p, int grid, void* stream);
-int launch_gram_tc_pair(const PhaseParams& p, int sm_count, void* stream);
-int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream);
+// cudaError_t as int.  pdl: launch as a programmatic dependent of the
+// previous kernel on the stream (every launch of a step but the first).
+int launch_momentum_norm(const EltParams& p, void* stream, bool pdl);
+int launch_norm_finalize(const EltParams& p, void* stream, bool pdl);
+int launch_apply(const EltParams& p, void* stream, bool pdl);
+int launch_gram_f32(const PhaseParams& p, void* stream, bool pdl);
+int launch_gemm_f32(const PhaseParams& p, void* stream, bool pdl);
+int launch_gram_tc(const PhaseParams& p, int grid, void* stream, bool pdl);
+int launch_gemm_tc(const PhaseParams& p, int grid, void* stream, bool pdl);
+int launch_gram_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool pdl);
+int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool pdl);
+
+// Programmatic dependent launch between the kernels of a step, unless built
+// with -DMUON_USE_PDL=0.
+#ifndef MUON_USE_PDL
+#define MUON_USE_PDL 1
+#endif
+constexpr bool kUsePdl = MUON_USE_PDL != 0;
 int tc_smem_bytes();
 
 // Tensor-core tile shape (used by the planner to count tiles): a CTA covers
