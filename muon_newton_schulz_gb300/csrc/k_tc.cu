@@ -104,7 +104,9 @@ struct Cfg {
   static constexpr int kBCols = kPair ? TN / 2 : TN;        // right-operand rows/columns per CTA
   static constexpr int kBBytes = kBCols * TK * 2;
   static constexpr int kStageBytes = A_BYTES + kBBytes;
-  // Gram: row-major and transposed 32x32 bf16 blocks, double-buffered (8 KiB).
+  // Gram: row-major and transposed 32x32 bf16 output blocks, double-buffered
+  // (Gram 1), or single-buffered beside two prefetched blocks of the previous
+  // A (Gram 2): 8 KiB.
   // GEMM: two input and two output buffers of (hi, lo) X boxes, 32 rows x
   // kGemmChunk bf16 each (8 or 16 KiB).
   static constexpr int kEpiWarpBytes = kGram ? 8192 : 8 * 32 * kGemmChunk * 2;
@@ -131,6 +133,31 @@ struct Tile { int g, mat, bi, bj; };
 #else
 #define TC_PROF_T0(v)
 #define TC_PROF_ADD(slot, v)
+#endif
+
+// Optional per-tile trace (build with -DMUON_TC_TRACE): clock64 stamps of the
+// leader CTA of each pair (or each CTA), per launch kind (0 Gram X X^T,
+// 1 Gram with the previous A, 2 GEMM; the last launch of a kind wins):
+//   [0] MMA issuer: accumulator granted     [1] MMA issuer: last MMA of the tile issued
+//   [2] epilogue warp 0: accumulator full   [3] epilogue warp 0: tile done
+// g_tc_life: CTA set-up done and CTA end.  Read with muon_tc_trace_read.
+#ifdef MUON_TC_TRACE
+constexpr int kTraceCtas = 160, kTraceTiles = 96;
+__device__ long long g_tc_trace[3][kTraceCtas][kTraceTiles][4];
+__device__ long long g_tc_life[3][kTraceCtas][2];
+#define TC_TRACE(k, slot)                                                                                       \
+  do {                                                                                                          \
+    const int kind_ = kGram ? (p.g[0].prev ? 1 : 0) : 2;                                                         \
+    if (blockIdx.x < kTraceCtas && (k) < kTraceTiles) g_tc_trace[kind_][blockIdx.x][(k)][(slot)] = clock64();   \
+  } while (0)
+#define TC_LIFE(slot)                                                                  \
+  do {                                                                                 \
+    const int kind_ = kGram ? (p.g[0].prev ? 1 : 0) : 2;                                \
+    if (blockIdx.x < kTraceCtas) g_tc_life[kind_][blockIdx.x][(slot)] = clock64();      \
+  } while (0)
+#else
+#define TC_TRACE(k, slot)
+#define TC_LIFE(slot)
 #endif
 
 // Flattened tile t -> (group, matrix, row block, column block).  Gram tiles
@@ -271,7 +298,9 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true, issued = false;
-  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits) {
+  int lt = 0;   // local tile count (trace)
+  (void)lt;
+  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits, ++lt) {
     const Tile tl = decode_tile<kPair>(p, t, kGram);
     const int nk = (p.g[tl.g].K + TK - 1) / TK;
     TC_PROF_T0(t_a);
@@ -280,6 +309,7 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
       break;
     }
     TC_PROF_ADD(2, t_a);
+    TC_TRACE(lt, 0);
     ptx::tc_fence_after();
     const uint32_t d = tmem_base + (uint32_t)(acc * TN);
     for (int kb = 0; kb < nk; ++kb) {
@@ -316,6 +346,7 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
     if (!ok) break;
     if (kPair) ptx::umma_commit_pair_mc(&tfull[acc], 0x3);
     else ptx::umma_commit(&tfull[acc]);
+    TC_TRACE(lt, 1);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
@@ -345,56 +376,63 @@ struct EpiCtx {
 
 // ---------------------------------------------------------------- Gram epilogue
 
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+    f[2 * h] = __low2float(b2);
+    f[2 * h + 1] = __high2float(b2);
+  }
+}
+
+
+// fp32 diagonal residuals of the previous A that one warp needs for a Gram-2
+// tile, loaded once per tile before the accumulator wait: lane l holds
+// R[col0 + 8 l .. col0 + 8 l + 7] (zero past m), and rr = R[row].
+struct GramDiag {
+  float rcv[8];
+  float rr;
+};
+
+__device__ __forceinline__ void gram_diag_load(const PhaseGroup& G, const Tile& tl, int lane, int row, int col0,
+                                               GramDiag& gd) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) gd.rcv[q] = 0.f;
+  gd.rr = 0.f;
+  if (!G.prev || !G.diag_in) return;
+  const float* rin = G.diag_in + (int64_t)tl.mat * G.diag_stride;
+  const int c = col0 + 8 * lane;
+  if (c + 8 <= G.m) {
+    const float4 q0 = *reinterpret_cast<const float4*>(rin + c);
+    const float4 q1 = *reinterpret_cast<const float4*>(rin + c + 4);
+    gd.rcv[0] = q0.x; gd.rcv[1] = q0.y; gd.rcv[2] = q0.z; gd.rcv[3] = q0.w;
+    gd.rcv[4] = q1.x; gd.rcv[5] = q1.y; gd.rcv[6] = q1.z; gd.rcv[7] = q1.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (c + q < G.m) gd.rcv[q] = rin[c + q];
+  }
+  if (row < G.m) gd.rr = rin[row];
+}
+
 // Gram values of one 32-column chunk for one row (fp32, before rounding).
 //   Gram 1 (no prev):  A = alpha * acc, alpha = s^2 in the first iteration.
 //   Gram 2 (prev = A): B = b * A + c * A^2 with A = A~ + R, A~ the stored bf16
-//     A and R the fp32 residual of its diagonal (diag_in):
+//     A (pa: this row's 32 values, from the prefetched block) and R the fp32
+//     residual of its diagonal (gd):
 //     A^2 = acc + A~ o (R_r + R_c) + R_r^2 on the diagonal, acc = A~ A~.
+// All lanes of the warp call this (the column residuals move by shuffles).
 __device__ __forceinline__ void gram_values(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, int row,
-                                            int c0, const uint32_t (&v)[32], float (&f)[32]) {
-  const int m = G.m;
-  const bool rv = row < m;
+                                            int c0, int col0, const uint32_t (&v)[32], const float (&pa)[32],
+                                            const GramDiag& gd, float (&f)[32]) {
   if (G.prev) {
-    const __nv_bfloat16* pr =
-        reinterpret_cast<const __nv_bfloat16*>(G.prev) + (int64_t)tl.mat * G.prev_stride + (int64_t)row * G.ld_prev + c0;
-    const float* rin = G.diag_in ? G.diag_in + (int64_t)tl.mat * G.diag_stride : nullptr;
-    float pa[32], rc[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) { pa[j] = 0.f; rc[j] = 0.f; }
-    if (rv && c0 + 32 <= m) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = *reinterpret_cast<const uint4*>(pr + 8 * i);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
-          pa[8 * i + 2 * h] = __low2float(b2);
-          pa[8 * i + 2 * h + 1] = __high2float(b2);
-        }
-      }
-    } else if (rv) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < m) pa[j] = __bfloat162float(pr[j]);
-    }
-    if (rin) {
-      if (c0 + 32 <= m) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 q = *reinterpret_cast<const float4*>(rin + c0 + 4 * i);
-          rc[4 * i] = q.x; rc[4 * i + 1] = q.y; rc[4 * i + 2] = q.z; rc[4 * i + 3] = q.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < m) rc[j] = rin[c0 + j];
-      }
-    }
-    const float rr = (rin && rv) ? rin[row] : 0.f;
+    const int src = (c0 - col0) >> 3;   // lane holding R[c0 .. c0 + 7]
+    const float rr = gd.rr;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      float acc = fmaf(pa[j], rr + rc[j], __uint_as_float(v[j]));
+      const float rc = __shfl_sync(0xffffffffu, gd.rcv[j & 7], src + (j >> 3));
+      float acc = fmaf(pa[j], rr + rc, __uint_as_float(v[j]));
       float aex = pa[j];
       if (c0 + j == row) {
         acc = fmaf(rr, rr, acc);
@@ -449,13 +487,20 @@ __device__ __forceinline__ void gram_store_diag_block(const PhaseParams& p, cons
 }
 
 // Chunk wholly above the diagonal: stage the 32 x 32 block and its transpose
-// in shared memory (double-buffered) and write both with TMA stores.
+// in shared memory and write both with TMA stores.  Staging per warp (8 KiB):
+// Gram 1 double-buffers the (block, transpose) pair at 0 / 2048 and
+// 4096 / 6144; Gram 2 has one pair at 0 / 2048 and its prefetched blocks of
+// the previous A at 4096 and 6144.
 __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, const Tile& tl, EpiCtx& ec, int r0,
-                                                       int c0, const float (&f)[32]) {
-  uint8_t* ro = ec.buf + ec.obuf * 2048;
-  uint8_t* tr = ec.buf + 4096 + ec.obuf * 2048;
+                                                       int c0, const float (&f)[32], bool single) {
+  const int o = single ? 0 : ec.obuf;
+  uint8_t* ro = ec.buf + o * 4096;
+  uint8_t* tr = ro + 2048;
   const int lane = ec.lane;
-  if (lane == 0) ptx::bulk_wait_read_1();   // the other buffer's stores may still read
+  if (lane == 0) {   // the stores that last read this buffer are done with it
+    if (single) ptx::bulk_wait_read_all();
+    else ptx::bulk_wait_read_1();
+  }
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -478,25 +523,86 @@ __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, con
     ptx::tma_store_4d(mc, tr, r0, c0, tl.mat, 0);
     ptx::bulk_commit();
   }
-  ec.obuf ^= 1;
+  if (!single) ec.obuf ^= 1;
 }
 
-__device__ __forceinline__ void gram_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
-                                                   EpiCtx& ec, uint32_t tbase, int r0, int col0) {
-  const int row = r0 + ec.lane;
-#pragma unroll 1
-  for (int ch = ec.slice; ch < TN / 32; ch += ec.nslices) {
-    const int c0 = col0 + ch * 32;
-    if (c0 >= G.m) break;        // uniform across the warp
-    if (c0 < r0) continue;       // wholly below the diagonal for this warp
-    uint32_t v[32];
-    ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), v);
-    ptx::tmem_ld_wait_regs(v);
-    float f[32];
-    gram_values(p, G, tl, row, c0, v, f);
-    if (c0 == r0) gram_store_diag_block(p, G, tl, row, c0, f);
-    else gram_store_upper_block(p, tl, ec, r0, c0, f);
+// Chunks of a Gram tile this warp handles: ch = first + k * nslices for
+// k < count, skipping chunks wholly below the diagonal (c0 < r0; r0 - col0 is
+// a multiple of 32) and past the last column.
+struct GramChunks { int first, count; };
+__device__ __forceinline__ GramChunks gram_chunks(const PhaseGroup& G, const EpiCtx& ec, int r0, int col0) {
+  const int lo = r0 > col0 ? (r0 - col0) / 32 : 0;
+  const int hi = min(TN / 32, (G.m - col0 + 31) / 32);
+  int first = ec.slice;
+  if (first < lo) first += (lo - first + ec.nslices - 1) / ec.nslices * ec.nslices;
+  const int count = first < hi ? (hi - first + ec.nslices - 1) / ec.nslices : 0;
+  return {first, count};
+}
+
+// Gram 2: TMA prefetch of the previous A's 32 x 32 block at (c0, r0) into
+// buffer b (completes on xfull[b]).
+__device__ __forceinline__ void gram_prefetch_prev(const PhaseParams& p, const Tile& tl, EpiCtx& ec, int b, int c0,
+                                                   int r0) {
+  if (ec.lane == 0) {
+    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2048u);
+    ptx::tma_load_4d(ec.buf + 4096 + 2048 * b, &p.map_d[tl.g], c0, r0, tl.mat, 0, &ec.xfull[b]);
   }
+}
+
+// One chunk of a Gram tile.  Returns false on a time-out.
+__device__ __forceinline__ bool gram_chunk(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, EpiCtx& ec,
+                                           const GramChunks& gc, int k, int r0, int col0, const uint32_t (&v)[32],
+                                           const GramDiag& gd, volatile int* abort) {
+  const int lane = ec.lane;
+  const int row = r0 + lane;
+  const int c0 = col0 + 32 * (gc.first + k * ec.nslices);
+  float pa[32];
+  if (G.prev) {
+    const int b = k & 1;
+    if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
+                                kWaitLimitNs))
+      return false;
+    ec.xphase ^= 1u << b;
+    const uint8_t* pb = ec.buf + 4096 + 2048 * b;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpack_bf16x8(*reinterpret_cast<const uint4*>(pb + ptx::sw64_off(lane, i)), pa + 8 * i);
+    __syncwarp();   // every lane has read buffer b: refill it
+    if (k + 2 < gc.count) gram_prefetch_prev(p, tl, ec, b, c0 + 64 * ec.nslices, r0);
+  }
+  float f[32];
+  gram_values(p, G, tl, row, c0, col0, v, pa, gd, f);
+  if (c0 == r0) gram_store_diag_block(p, G, tl, row, c0, f);
+  else gram_store_upper_block(p, tl, ec, r0, c0, f, G.prev != nullptr);
+  return true;
+}
+
+// The Gram tile's epilogue for this warp; the TMEM load of chunk k + 1 is in
+// flight while chunk k is processed.
+__device__ __forceinline__ bool gram_tile_epilogue(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
+                                                   EpiCtx& ec, uint32_t tbase, int r0, int col0,
+                                                   const GramChunks& gc, const GramDiag& gd, volatile int* abort) {
+  if (gc.count <= 0) return true;
+  uint32_t va[32], vb[32];
+  ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * gc.first), va);
+  ptx::tmem_ld_wait_regs(va);
+#pragma unroll 1
+  for (int k = 0; k < gc.count; k += 2) {
+    const bool has1 = k + 1 < gc.count;
+    if (has1) ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * (gc.first + (k + 1) * ec.nslices)), vb);
+    if (!gram_chunk(p, G, tl, ec, gc, k, r0, col0, va, gd, abort)) {
+      if (has1) ptx::tmem_ld_wait_regs(vb);
+      return false;
+    }
+    if (has1) {
+      ptx::tmem_ld_wait_regs(vb);
+      const bool has2 = k + 2 < gc.count;
+      if (has2) ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * (gc.first + (k + 2) * ec.nslices)), va);
+      const bool okb = gram_chunk(p, G, tl, ec, gc, k + 1, r0, col0, vb, gd, abort);
+      if (has2) ptx::tmem_ld_wait_regs(va);
+      if (!okb) return false;
+    }
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------- GEMM epilogue
@@ -536,16 +642,6 @@ __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseG
       if (ae->d.tall) ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, r0, c0, &ec.xfull[b]);
       else ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, c0, r0, &ec.xfull[b]);
     }
-  }
-}
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
-    f[2 * h] = __low2float(b2);
-    f[2 * h + 1] = __high2float(b2);
   }
 }
 
@@ -743,13 +839,26 @@ __device__ __forceinline__ void run_epilogue(const PhaseParams& p, const PairInf
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true;
-  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits) {
+  int lt = 0;   // local tile count (trace)
+  (void)lt;
+  const bool tracer = ec.quarter == 0 && ec.slice == 0 && ec.lane == 0 && pi.rank == 0;
+  (void)tracer;
+  for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits, ++lt) {
     const Tile tl = decode_tile<kPair>(p, t, kGram);
     const PhaseGroup& G = p.g[tl.g];
     const int r0 = tl.bi * C::kTileM + TC * pi.rank + ec.quarter * 32;   // first row of this warp
     const int col0 = tl.bj * TN;
     int cnt = 0;
-    if (!kGram) {
+    GramChunks gc{0, 0};
+    GramDiag gd;
+    if (kGram) {
+      gc = gram_chunks(G, ec, r0, col0);
+      gram_diag_load(G, tl, ec.lane, r0 + ec.lane, col0, gd);
+      if (G.prev) {
+        cnt = gc.count;
+        for (int k = 0; k < 2 && k < cnt; ++k) gram_prefetch_prev(p, tl, ec, k, col0 + 32 * (gc.first + k * ec.nslices), r0);
+      }
+    } else {
       const int nch = min(TN / kGC, (G.n - col0 + kGC - 1) / kGC);
       cnt = nch > ec.slice ? (nch - ec.slice + ec.nslices - 1) / ec.nslices : 0;
       // the W tensor map was written to global memory by the momentum kernel
@@ -761,19 +870,21 @@ __device__ __forceinline__ void run_epilogue(const PhaseParams& p, const PairInf
 #ifdef MUON_TC_PROFILE
     if (ec.lane == 0) TC_PROF_ADD(4, t_t);
 #endif
+    if (tracer) TC_TRACE(lt, 2);
     if (ok) {
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(ec.quarter * 32) << 16) + (uint32_t)(acc * TN);
-      if (kGram) gram_tile_epilogue(p, G, tl, ec, tbase, r0, col0);
+      if (kGram) ok = gram_tile_epilogue(p, G, tl, ec, tbase, r0, col0, gc, gd, abort);
       else ok = gemm_tile_epilogue(p, G, tl, ec, tbase, r0, col0, cnt, abort);
     }
     if (!ok) {
-      // let this warp's X prefetches in flight land before the CTA can exit
-      if (!kGram)
-        for (int b = 0; b < 2; ++b)
-          if (b < cnt) wait_drain(&ec.xfull[b], (ec.xphase >> b) & 1u);
+      // let this warp's prefetches in flight (X, or the previous A) land
+      // before the CTA can exit
+      for (int b = 0; b < 2; ++b)
+        if (b < cnt) wait_drain(&ec.xfull[b], (ec.xphase >> b) & 1u);
       break;
     }
+    if (tracer) TC_TRACE(lt, 3);
     ptx::tc_fence_before();
     if (kPair) {
       // one arrival per warp, on the even CTA's barrier
@@ -836,10 +947,8 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
     for (int g = 0; g < p.ngroups; ++g) {
       ptx::prefetch_tmap(&p.map_a[g]);
       ptx::prefetch_tmap(&p.map_c[g]);
-      if (!kGram) {
-        ptx::prefetch_tmap(&p.map_b[g]);
-        ptx::prefetch_tmap(&p.map_d[g]);
-      }
+      if (!kGram) ptx::prefetch_tmap(&p.map_b[g]);
+      if (!kGram || p.g[g].prev) ptx::prefetch_tmap(&p.map_d[g]);
     }
   }
   if (warp == 1) {
@@ -860,6 +969,7 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
   // of the step produced
   grid_dependency_wait();
   if (threadIdx.x == 0) allow_dependent_launch();
+  if (threadIdx.x == 0) TC_LIFE(0);
 
   if (warp == 0) {
     if (lane == 0) run_producer<kGram, kPair>(p, pi, smem, full, empty, abort);
@@ -894,6 +1004,7 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
 #ifdef MUON_TC_PROFILE
   if (threadIdx.x == 0) TC_PROF_ADD(5, t_cta);
 #endif
+  if (threadIdx.x == 0) TC_LIFE(1);
 }
 
 template <bool kGram>
@@ -962,3 +1073,21 @@ int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool p
 }
 
 }  // namespace muon
+
+#ifdef MUON_TC_TRACE
+// Trace reader of -DMUON_TC_TRACE builds: copies g_tc_trace then g_tc_life
+// into dst (bytes >= their sizes) and clears both.
+extern "C" int muon_tc_trace_read(void* dst, size_t bytes) {
+  const size_t a = sizeof(muon::g_tc_trace), b = sizeof(muon::g_tc_life);
+  if (bytes < a + b) return -1;
+  if (cudaMemcpyFromSymbol(dst, muon::g_tc_trace, a) != cudaSuccess) return -2;
+  if (cudaMemcpyFromSymbol(static_cast<char*>(dst) + a, muon::g_tc_life, b) != cudaSuccess) return -3;
+  void* pa = nullptr;
+  void* pb = nullptr;
+  if (cudaGetSymbolAddress(&pa, muon::g_tc_trace) != cudaSuccess) return -4;
+  if (cudaGetSymbolAddress(&pb, muon::g_tc_life) != cudaSuccess) return -4;
+  cudaMemset(pa, 0, a);
+  cudaMemset(pb, 0, b);
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
+}
+#endif

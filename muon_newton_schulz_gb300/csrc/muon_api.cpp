@@ -728,8 +728,11 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
                    encode_map(h, mc, Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else if (phase == 1) {
+              // map_d: 32 x 32 blocks of A itself, prefetched by the epilogue
               ok = encode_map(h, ma, Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 64, 128) &&
                    encode_map(h, mc, Bbuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
+                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                   encode_map(h, md, Abuf, G.m, G.m, cnt, 1, arow, amat, amat * cnt, 32, 32,
                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
             } else {
               // epilogue boxes: 32 rows x kGemmChunk bf16 (32- or 64-byte rows)

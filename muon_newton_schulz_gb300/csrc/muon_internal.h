@@ -113,7 +113,7 @@ struct PhaseParams {
   CUtensorMap map_a[kMaxGroups];   // tensor-core path: left operand (and Gram right operand)
   CUtensorMap map_b[kMaxGroups];   // tensor-core path: GEMM right operand (MN-major X)
   CUtensorMap map_c[kMaxGroups];   // epilogue: Gram output (bf16, 32x32 box) / GEMM X hi in+out (32 rows x chunk)
-  CUtensorMap map_d[kMaxGroups];   // epilogue: GEMM X lo in+out (32 rows x chunk)
+  CUtensorMap map_d[kMaxGroups];   // epilogue: Gram 2 previous A (32x32 box) / GEMM X lo in+out (32 rows x chunk)
   PhaseGroup g[kMaxGroups];
   int32_t ngroups;
   int32_t total_tiles;
