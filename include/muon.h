@@ -61,8 +61,9 @@ typedef enum {
 typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
 
 typedef enum {
-    /* bf16 tensor-core operands, fp32 accumulation, fp32 master copy of X,
-       A and (bA + cA^2) stored bf16 */
+    /* bf16 tensor-core operands, fp32 accumulation; X kept as the bf16 pair
+       hi = bf16(x), lo = bf16(x - hi); A and (bA + cA^2) stored bf16 with
+       their diagonals in fp32 */
     MUON_MODE_BF16 = 0,
     /* fp32 operands on the CUDA cores throughout: the validation mode */
     MUON_MODE_FP32_VALIDATE = 1
@@ -76,6 +77,9 @@ typedef struct {
     int32_t ns_iters;   /* Newton-Schulz iterations, 0..64, default 5 */
     int32_t nesterov;   /* 0: NS input is the new momentum; 1: G + beta * (new momentum) */
     int32_t mode;       /* muon_mode, default MUON_MODE_BF16 */
+    int32_t dampening;  /* 0 (default): M <- beta*M + G; 1: M <- beta*M + (1 - beta)*G, the
+                           moving-average form, and the Nesterov input (1 - beta)*G + beta*M.
+                           The pages fix neither form; the second is a variant. */
 } muon_config;
 
 /* One whole weight matrix, rows x cols, every buffer row-major with its own

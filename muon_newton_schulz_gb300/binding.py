@@ -36,6 +36,7 @@ class muon_config(ctypes.Structure):
         ("beta", c_float), ("a", c_float), ("b", c_float), ("c", c_float),
         ("eps", c_float), ("scale_coeff", c_float),
         ("ns_iters", c_int32), ("nesterov", c_int32), ("mode", c_int32),
+        ("dampening", c_int32),
     ]
 
 
@@ -194,10 +195,11 @@ class MuonStep:
     tensors (device memory owned by torch) on the current stream."""
 
     def __init__(self, device: int = 0, beta=0.95, a=3.4445, b=-4.7750, c=2.0315, eps=1e-7,
-                 scale_coeff=0.2, ns_iters=5, nesterov=False, mode=MUON_MODE_BF16):
+                 scale_coeff=0.2, ns_iters=5, nesterov=False, mode=MUON_MODE_BF16, dampening=False):
         cfg = muon_config_default()
         cfg.beta, cfg.a, cfg.b, cfg.c, cfg.eps, cfg.scale_coeff = beta, a, b, c, eps, scale_coeff
         cfg.ns_iters, cfg.nesterov, cfg.mode = int(ns_iters), 1 if nesterov else 0, int(mode)
+        cfg.dampening = 1 if dampening else 0
         st, h = muon_create(cfg, device)
         if st != MUON_OK:
             raise MuonError(st, f"muon_create(device={device})")

@@ -97,7 +97,10 @@ __device__ __forceinline__ void load_x4(const EltMat& e, int64_t off, float (&v)
 }
 
 // ---------------------------------------------------------------- K1
-// M <- beta*M + G (fp32 fma, in place); X0 = M (or G + beta*M with Nesterov)
+// M <- beta*M + G (fp32 fma, in place); X0 = M (or G + beta*M with Nesterov).
+// With dampening the gradient term is (1 - beta)*G, formed exactly as p + e
+// (p = fl(d*G), e = fma(d, G, -p), d = 1 - beta exact in fp32), so that
+// M = fma(beta, M, p) + e stays within one rounding of beta*M + (1 - beta)*G.
 // written in wide orientation (fp32, or as the bf16 hi/lo pair); one fp64
 // sum of squares of X0 per tile.  The normalisation 1/(||X0||+eps) is not
 // applied here: it is folded into the first iteration's epilogues.
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constan
   const int c0 = (int)(lt % e.tiles_c) * kT;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const float beta = p.beta;
+  const float damp = 1.f - beta;   // exact for beta in [0.5, 2] (Sterbenz)
   float ss = 0.f;
   double ssd = 0.0;
 
@@ -159,8 +163,15 @@ __global__ void __launch_bounds__(kThreads) k_momentum_norm(const __grid_constan
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      mm[q] = fmaf(beta, mm[q], g[q]);
-      x[q] = p.nesterov ? fmaf(beta, mm[q], g[q]) : mm[q];
+      if (p.dampening) {
+        const float gp = damp * g[q];
+        const float ge = fmaf(damp, g[q], -gp);
+        mm[q] = fmaf(beta, mm[q], gp) + ge;
+        x[q] = p.nesterov ? fmaf(beta, mm[q], gp) + ge : mm[q];
+      } else {
+        mm[q] = fmaf(beta, mm[q], g[q]);
+        x[q] = p.nesterov ? fmaf(beta, mm[q], g[q]) : mm[q];
+      }
       ss = fmaf(x[q], x[q], ss);
     }
     if (vec) {

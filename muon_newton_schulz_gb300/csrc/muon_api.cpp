@@ -97,6 +97,7 @@ muon_status check_config(const muon_config& c, std::string& why) {
   if (c.eps < 0.f) { why = "config: eps must be >= 0"; return MUON_ERR_INVALID_ARG; }
   if (c.ns_iters < 0 || c.ns_iters > kMaxIters) { why = "config: ns_iters must be in [0, 64]"; return MUON_ERR_INVALID_ARG; }
   if (c.nesterov != 0 && c.nesterov != 1) { why = "config: nesterov must be 0 or 1"; return MUON_ERR_INVALID_ARG; }
+  if (c.dampening != 0 && c.dampening != 1) { why = "config: dampening must be 0 or 1"; return MUON_ERR_INVALID_ARG; }
   if (c.mode != MUON_MODE_BF16 && c.mode != MUON_MODE_FP32_VALIDATE) { why = "config: unknown mode"; return MUON_ERR_UNSUPPORTED; }
   return MUON_OK;
 }
@@ -354,6 +355,7 @@ void muon_config_default(muon_config* c) {
   c->scale_coeff = 0.2f;
   c->ns_iters = 5;
   c->nesterov = 0;
+  c->dampening = 0;
   c->mode = MUON_MODE_BF16;
 }
 
@@ -561,6 +563,7 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
     std::memset(&ep, 0, sizeof(ep));
     ep.nmats = (int32_t)(e - b);
     ep.nesterov = cfg.nesterov;
+    ep.dampening = cfg.dampening;
     ep.apply_scale = iters == 0 ? 1 : 0;
     ep.beta = cfg.beta;
     ep.eps = cfg.eps;

@@ -76,6 +76,7 @@ struct EltParams {
   EltMat mats[kMaxEltMats];
   int32_t nmats;
   int32_t nesterov;
+  int32_t dampening;       // 1: the gradient enters the momentum as (1 - beta) * G
   int32_t apply_scale;     // apply: multiply O by scale[] (zero iterations)
   float beta;
   float eps;

@@ -94,6 +94,13 @@ WORKLOADS = {
         MatrixSpec(300, 8, 1, "gauss", 1.0),
         MatrixSpec(264, 1000, 1, "gauss", 1e-3),
     ), seed_base=16000),
+    # more shape groups than one Newton-Schulz launch takes (21 > 16) and more
+    # matrices than one momentum launch takes (70 > 64): every phase runs as a
+    # chain of launches
+    "many_groups": Workload("many_groups", tuple(
+        MatrixSpec(8 + 8 * k, 3 * (8 + 8 * k) + 8, 1, "gauss", 1.0) if k % 2 == 0
+        else MatrixSpec(3 * (8 + 8 * k) + 8, 8 + 8 * k, 1, "gauss", 1.0)
+        for k in range(20)) + (MatrixSpec(16, 48, 50, "gauss", 1.0),), seed_base=17000),
 }
 
 # The workload the throughput metric is quoted on.

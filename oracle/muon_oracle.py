@@ -33,7 +33,9 @@ Readings where the pages are silent (each also listed in the design notes):
      iteration; R2 momentum ``beta*M + G`` without dampening, beta = 0.95;
   R3 no Nesterov by default; with ``nesterov`` the NS input is
      ``G + beta*M`` (new M), the usual Nesterov form; R4 eps = 1e-7 added to the norm; R5 transpose iff
-  rows > cols; R6 no weight decay; R7 bf16 weights rounded RN-even.
+  rows > cols; R6 no weight decay; R7 bf16 weights rounded RN-even;
+  R17 (a variant, off by default) ``dampening``: ``M <- beta*M + (1-beta)*G``
+     and the Nesterov input ``(1-beta)*G + beta*M``.
 
 Pins (tests/test_oracle_pins.py): the singular-value polynomial closed form
 via SVD, convergence to the polar factor with (1.5, -0.5, 0) against
@@ -67,14 +69,20 @@ class OracleConfig:
     scale_coeff: float = 0.2
     ns_iters: int = 5
     nesterov: bool = False
+    dampening: bool = False
 
 
-def momentum(M: np.ndarray, G: np.ndarray, beta: float) -> np.ndarray:
+def momentum(M: np.ndarray, G: np.ndarray, beta: float, dampening: bool = False) -> np.ndarray:
     """Step 1: ``beta*M + G`` evaluated in fp64 from the fp32 inputs and
     rounded once to fp32.  beta*M is exact in fp64 (24+24 bit product), so this
     equals the correctly rounded fused multiply-add except in double-rounding
-    corner cases."""
-    out = float(beta) * M.astype(np.float64) + G.astype(np.float64)
+    corner cases.  With ``dampening`` (reading R17) the gradient enters as
+    ``(1 - beta)*G``, the moving-average form; 1 - beta is exact for the fp32
+    beta and its product with G is exact in fp64 too."""
+    g = G.astype(np.float64)
+    if dampening:
+        g = (1.0 - float(beta)) * g
+    out = float(beta) * M.astype(np.float64) + g
     return out.astype(np.float32)
 
 
@@ -166,10 +174,11 @@ def muon_step_matrix(W: np.ndarray, G: np.ndarray, M: np.ndarray, lr: float,
                      cfg: OracleConfig = OracleConfig(), w_is_bf16: bool = False) -> OracleStepResult:
     """Steps 1-6 for one matrix.  ``W`` is float32 (holding bf16 values when
     ``w_is_bf16``), ``G`` and ``M`` float32, all rows x cols."""
-    M_new = momentum(M, G, cfg.beta)
+    M_new = momentum(M, G, cfg.beta, cfg.dampening)
     src = M_new
     if cfg.nesterov:
-        src = G.astype(np.float64) + float(cfg.beta) * M_new.astype(np.float64)
+        gin = (1.0 - float(cfg.beta)) * G.astype(np.float64) if cfg.dampening else G.astype(np.float64)
+        src = gin + float(cfg.beta) * M_new.astype(np.float64)
     X, transposed = orient(src)
     X0 = frobenius_normalise(X, cfg.eps)
     Xk = newton_schulz(X0, cfg.a, cfg.b, cfg.c, cfg.ns_iters)

@@ -32,7 +32,8 @@ def f32_ulps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(ia - ib)
 
 
-def run_gpu(Ws, Gs, Ms, lrs, mode=B.MUON_MODE_BF16, ns_iters=5, nesterov=False, export_o=True, runner=None):
+def run_gpu(Ws, Gs, Ms, lrs, mode=B.MUON_MODE_BF16, ns_iters=5, nesterov=False, export_o=True, runner=None,
+            dampening=False):
     """Copies the host tensors to the GPU, runs one step and returns host
     copies (W, M, O lists).  Inputs are not modified."""
     dev = torch.device("cuda", DEV)
@@ -40,7 +41,7 @@ def run_gpu(Ws, Gs, Ms, lrs, mode=B.MUON_MODE_BF16, ns_iters=5, nesterov=False, 
     Gd = [g.to(dev).contiguous() for g in Gs]
     Md = [m.to(dev).contiguous() for m in Ms]
     Od = [torch.full(w.shape, float("nan"), dtype=torch.float32, device=dev) for w in Ws] if export_o else None
-    ms = runner or B.MuonStep(DEV, ns_iters=ns_iters, nesterov=nesterov, mode=mode)
+    ms = runner or B.MuonStep(DEV, ns_iters=ns_iters, nesterov=nesterov, mode=mode, dampening=dampening)
     ms.step(Wd, Gd, Md, lrs, Od)
     torch.cuda.synchronize(dev)
     assert ms.check_status() == B.MUON_OK
@@ -50,8 +51,8 @@ def run_gpu(Ws, Gs, Ms, lrs, mode=B.MUON_MODE_BF16, ns_iters=5, nesterov=False, 
     return out
 
 
-def oracle_for(W, G, M, lr, ns_iters=5, nesterov=False):
-    cfg = O.OracleConfig(ns_iters=ns_iters, nesterov=nesterov) if nesterov else O.OracleConfig(ns_iters=ns_iters)
+def oracle_for(W, G, M, lr, ns_iters=5, nesterov=False, dampening=False):
+    cfg = O.OracleConfig(ns_iters=ns_iters, nesterov=nesterov, dampening=dampening)
     return O.muon_step_matrix(W.float().numpy(), G.numpy(), M.numpy(), lr, cfg, w_is_bf16=(W.dtype == torch.bfloat16))
 
 
@@ -87,14 +88,16 @@ def check_matrix(W0, G, M0, lr, Wg, Mg, Og, res, tol_o, mode_name=""):
 
 
 def run_and_check(workload_name, mode=B.MUON_MODE_BF16, tol_o=2e-2, ns_iters=5, indices=None, nesterov=False,
-                  steady_momentum=False):
+                  steady_momentum=False, runner=None, dampening=False):
     w = wl.WORKLOADS[workload_name]
     Ws, Gs, Ms, lrs = wl.make_workload(w, "cpu", steady_momentum=steady_momentum, indices=indices)
-    Wg, Mg, Og = run_gpu(Ws, Gs, Ms, lrs, mode=mode, ns_iters=ns_iters, nesterov=nesterov)
+    Wg, Mg, Og = run_gpu(Ws, Gs, Ms, lrs, mode=mode, ns_iters=ns_iters, nesterov=nesterov, runner=runner,
+                         dampening=dampening)
     errs = []
     for i in range(len(Ws)):
-        res = oracle_for(Ws[i], Gs[i], Ms[i], lrs[i], ns_iters, nesterov)
+        res = oracle_for(Ws[i], Gs[i], Ms[i], lrs[i], ns_iters, nesterov, dampening)
         errs.append(check_matrix(Ws[i], Gs[i], Ms[i], lrs[i], Wg[i], Mg[i], Og[i], res, tol_o,
                                  f"{workload_name}[{i}]"))
-    print(f"\nERR {workload_name} mode={mode} iters={ns_iters} nesterov={nesterov} max_rel_err={max(errs):.3e}")
+    print(f"\nERR {workload_name} mode={mode} iters={ns_iters} nesterov={nesterov} dampening={dampening} "
+          f"max_rel_err={max(errs):.3e}")
     return errs

@@ -41,12 +41,13 @@ def test_config_defaults(lib):
     assert abs(c.beta - 0.95) < 1e-7 and c.ns_iters == 5 and c.mode == B.MUON_MODE_BF16
     assert (round(c.a, 4), round(c.b, 4), round(c.c, 4)) == (3.4445, -4.775, 2.0315)
     assert abs(c.scale_coeff - 0.2) < 1e-7 and abs(c.eps - 1e-7) < 1e-12
+    assert c.nesterov == 0 and c.dampening == 0
 
 
 def test_struct_layout_matches_header(lib):
     # 2 x int64, then pointer/int32/int32/int64, ... as declared
     assert ctypes.sizeof(B.muon_matrix_desc) == 8 * 2 + 8 + 4 + 4 + 8 + 8 * 2 + 8 * 2 + 4 + 4 + 8 * 2
-    assert ctypes.sizeof(B.muon_config) == 9 * 4
+    assert ctypes.sizeof(B.muon_config) == 10 * 4
 
 
 @pytest.fixture()
@@ -151,6 +152,7 @@ def test_negative_n(host_handle):
     ("ns_iters", -1, B.MUON_ERR_INVALID_ARG),
     ("mode", 7, B.MUON_ERR_UNSUPPORTED),
     ("nesterov", 2, B.MUON_ERR_INVALID_ARG),
+    ("dampening", -1, B.MUON_ERR_INVALID_ARG),
     ("eps", -1.0, B.MUON_ERR_INVALID_ARG),
     ("beta", float("inf"), B.MUON_ERR_INVALID_ARG),
 ])

@@ -42,3 +42,29 @@ def test_nesterov(mode):
 def test_steady_state_momentum(mode):
     tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
     run_and_check("ragged_h384", mode=mode, tol_o=tol, steady_momentum=True)
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_phases_split_over_launches(mode):
+    """21 shape groups and 70 matrices: each Newton-Schulz phase takes two
+    launches (16 + 5 groups) and the momentum pass two (64 + 6 matrices); the
+    chained launches must give every matrix the oracle's result."""
+    tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
+    runner = B.MuonStep(0, mode=mode)
+    before = B.muon_launch_count(runner.h)
+    errs = run_and_check("many_groups", mode=mode, tol_o=tol, runner=runner)
+    launches = B.muon_launch_count(runner.h) - before
+    runner.close()
+    assert max(errs) <= tol
+    # momentum + finalize per chunk, 3 phases x 5 iterations x 2 launches,
+    # and (validation mode) a separate apply per chunk
+    assert launches == 2 * 2 + 3 * 5 * 2 + (2 if mode == B.MUON_MODE_FP32_VALIDATE else 0)
+
+
+@pytest.mark.parametrize("nesterov", [False, True])
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_dampened_momentum(mode, nesterov):
+    """The moving-average momentum variant (1 - beta) G, from a mid-training
+    momentum state: M within one fp32 ulp of the oracle, O within tolerance."""
+    tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
+    run_and_check("ragged_h384", mode=mode, tol_o=tol, nesterov=nesterov, dampening=True, steady_momentum=True)

@@ -381,3 +381,65 @@ def test_nesterov_from_zero_momentum_is_a_rescaling():
     b = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig(nesterov=True))
     assert _rel(a.O, b.O) > 1e-3
     assert np.array_equal(a.M, b.M)
+
+
+def test_dampened_momentum_closed_form_and_fixed_point():
+    """With dampening the momentum is the moving average
+    (1 - beta) * sum_k beta^(t-1-k) G_k; a constant gradient G gives
+    (1 - beta^t) G, which tends to G (reading R17)."""
+    r = _rng(63)
+    beta = float(np.float32(0.95))
+    Gs = [r.standard_normal((4, 6)).astype(np.float32) for _ in range(6)]
+    M = np.zeros((4, 6), np.float32)
+    for G in Gs:
+        M = O.momentum(M, G, beta, dampening=True)
+    t = len(Gs)
+    want = (1.0 - beta) * sum(beta ** (t - 1 - k) * Gs[k].astype(np.float64) for k in range(t))
+    assert np.abs(M - want).max() <= 8 * np.finfo(np.float32).eps * np.abs(want).max()
+    G = r.standard_normal((3, 5)).astype(np.float32)
+    M = np.zeros_like(G)
+    for _ in range(40):
+        M = O.momentum(M, G, beta, dampening=True)
+    want = (1.0 - beta ** 40) * G.astype(np.float64)
+    assert np.abs(M - want).max() <= 64 * np.finfo(np.float32).eps * np.abs(G).max()
+
+
+def test_dampened_momentum_is_a_single_rounding():
+    """beta*M + (1 - beta)*G is exact in fp64 for fp32 inputs (1 - beta has 20
+    significant bits), so the oracle's fp32 value is the nearest one."""
+    r = _rng(64)
+    beta = float(np.float32(0.95))
+    M = r.standard_normal(200).astype(np.float32)
+    G = r.standard_normal(200).astype(np.float32)
+    got = O.momentum(M, G, beta, dampening=True)
+    d = Fraction(1) - Fraction(beta)
+    for i in range(200):
+        exact = Fraction(beta) * Fraction(float(M[i])) + d * Fraction(float(G[i]))
+        cand = np.float32(float(exact))
+        lo, hi = np.nextafter(cand, np.float32(-np.inf)), np.nextafter(cand, np.float32(np.inf))
+        best = min((cand, lo, hi), key=lambda v: abs(Fraction(float(v)) - exact))
+        assert got[i] == best
+
+
+def test_dampened_nesterov_input():
+    """Dampening and Nesterov together: the NS input is (1 - beta) G + beta M_new;
+    from a zero momentum that is (1 - beta)(1 + beta) G up to the fp32 rounding
+    of the stored M_new = fl((1 - beta) G), a positive multiple of G, so the
+    update equals the plain one (eps = 0) to about fp32 precision."""
+    G = _rng(65).standard_normal((6, 10)).astype(np.float32)
+    Z = np.zeros_like(G)
+    plain = O.muon_step_matrix(Z, G, Z, 0.0, O.OracleConfig(eps=0.0))
+    both = O.muon_step_matrix(Z, G, Z, 0.0, O.OracleConfig(eps=0.0, nesterov=True, dampening=True))
+    assert _rel(both.O, plain.O) < 1e-6
+    # a dropped (1 - beta) on the gradient term would still be a multiple of G
+    # here, so the non-zero-momentum check below is the one that pins the form
+    M = _rng(66).standard_normal((6, 10)).astype(np.float32)
+    a = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig(dampening=True))
+    b = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig(dampening=True, nesterov=True))
+    beta = float(np.float32(0.95))
+    # the dampened momentum itself, and the Nesterov input built from it
+    assert np.array_equal(a.M, O.momentum(M, G, beta, dampening=True))
+    src = (1.0 - beta) * G.astype(np.float64) + beta * a.M.astype(np.float64)
+    X0 = O.frobenius_normalise(src, 1e-7)
+    want = O.newton_schulz(X0, O.NS_A, O.NS_B, O.NS_C, 5)
+    assert _rel(b.O, want) < 1e-12
