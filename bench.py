@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunk", type=int, default=2)
+    ap.add_argument("--e2e-chunk", type=int, default=1)
+    ap.add_argument("--e2e-slots", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -354,7 +355,7 @@ def run_gb300(args):
         Mh = [x.cpu().pin_memory() for x in Ms]
         h2d = sum(x.numel() * x.element_size() for x in Wh + Gh + Mh)
         d2h = sum(x.numel() * x.element_size() for x in Wh + Mh)
-        off = HostOffloadedMuon(local, chunk=args.e2e_chunk, slots=3, mode=mode)
+        off = HostOffloadedMuon(local, chunk=args.e2e_chunk, slots=args.e2e_slots, mode=mode)
         off.step(Wh, Gh, Mh, lrs)           # warm-up: allocates the slot buffers
         torch.cuda.synchronize(dev)
         barrier()
@@ -370,7 +371,8 @@ def run_gb300(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             dt = float(t.item())
         e2e = {"value": total_mats / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": dt * 1e3, "pipeline": f"chunks of {args.e2e_chunk} matrices, 3 device slots"}
+               "ms_per_step": dt * 1e3,
+               "pipeline": f"chunks of {args.e2e_chunk} matrices, {args.e2e_slots} device slots"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
