@@ -81,11 +81,16 @@ def measured_traffic(workload: str):
 
 
 def peaks():
+    """(bf16 burst TF/s, bf16 sustained TF/s, HBM GB/s, kind).  The kernels
+    are timed inside a long run of back-to-back steps, under the power cap, so
+    the sustained figure is the roofline's denominator; the burst one is
+    reported beside it."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
-    return 1900.0, 6800.0, "fallback"
+        burst = float(d["bf16_tflops"])
+        return burst, float(d.get("bf16_tflops_sustained", burst)), float(d["hbm_gbs"]), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
 
 
 class ClockSampler:
@@ -322,7 +327,7 @@ def run_gb300(args):
     value = total_mats / (ms_step / 1e3)
     sym_flops = wl.workload_flops(w)
     dense_flops = wl.workload_flops(w, symmetric=False)
-    peak_tf, hbm_gbs, peak_kind = peaks()
+    burst_tf, peak_tf, hbm_gbs, peak_kind = peaks()
 
     # dominant kernel: the GEMM with the a X epilogue (61% of the flops)
     gemm_flops = sum(2.0 * min(r, c) ** 2 * max(r, c) for r, c in w.shapes)
@@ -341,6 +346,7 @@ def run_gb300(args):
         wbytes = 2 if name != "single_256x512" else 4
         k5_bytes = elems * (4 + 2 * wbytes)          # read X (hi + lo); read + write W
         phase["momentum_norm"]["gbs"] = k1_bytes / (phase["momentum_norm"]["ms_per_step"] / 1e3) / 1e9
+        phase["momentum_norm"]["frac_of_hbm"] = phase["momentum_norm"]["gbs"] / hbm_gbs
         if phase["apply"]["launches_per_step"] > 0:
             phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
 
@@ -387,14 +393,18 @@ def run_gb300(args):
         "vs_baseline": None, "dtype": "bf16" if mode == B.MUON_MODE_BF16 else "f32", "data": "synthetic",
         "config": {"workload": name, "matrices_per_gpu": w.n_matrices, "shapes": sorted(set(w.shapes)),
                    "ns_iters": 5, "parallelism": f"replicas x{world} (whole matrices per rank)",
-                   "l2": "inputs larger than L2: 16 x 2048x8192 fp32 G, M and the 1.5 GB of X per step"
+                   "l2": "inputs larger than L2: 16 x 2048x8192 fp32 G, M and the 1.07 GB of X (hi, lo) per step"
                    if name == wl.HEADLINE else "see workload sizes"},
         "tflops_symmetric": sym_flops / (ms_step / 1e3) / 1e12 * world,
         "tflops_dense_equivalent": dense_flops / (ms_step / 1e3) / 1e12 * world,
         "frac_of_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / peak_tf,
+        "frac_of_burst_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / burst_tf,
         "roofline": {"kernel": "k_ns_tc_pair<GEMM> (gemm_update)", "bound": "tensor", "achieved": achieved,
-                     "peak": peak_tf, "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf if achieved is not None else None, "traffic": traffic,
+                     "peak": peak_tf, "peak_kind": f"{peak_kind} bf16 sustained (timed inside back-to-back steps, "
+                                                   f"under the power cap)",
+                     "burst_peak": burst_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf if achieved is not None else None,
+                     "frac_of_burst": achieved / burst_tf if achieved is not None else None, "traffic": traffic,
                      "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": gemm_ms},
         "phases": phase,
         "e2e": e2e,
