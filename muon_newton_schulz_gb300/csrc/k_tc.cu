@@ -137,27 +137,52 @@ struct Tile { int g, mat, bi, bj; };
 
 // Optional per-tile trace (build with -DMUON_TC_TRACE): clock64 stamps of the
 // leader CTA of each pair (or each CTA), per launch kind (0 Gram X X^T,
-// 1 Gram with the previous A, 2 GEMM; the last launch of a kind wins):
+// 1 Gram with the previous A, 2 GEMM, 3 GEMM that applies the update; the
+// last launch of a kind wins):
 //   [0] MMA issuer: accumulator granted     [1] MMA issuer: last MMA of the tile issued
 //   [2] epilogue warp 0: accumulator full   [3] epilogue warp 0: tile done
-// g_tc_life: CTA set-up done and CTA end.  Read with muon_tc_trace_read.
+// g_tc_life: CTA set-up done and CTA end.
+// g_tc_epi: cycles the tracing epilogue warp (lane 0 of warp quarter 0 of the
+// leader) spends in [0] X-prefetch waits, [1] waits for its previous TMA
+// store to release the staging buffer, [2] TMEM load waits (GEMM).
+// g_tc_mma: cycles the MMA issuer waits for a full stage: [0] on the tile's
+// first k-block, [1] on its first four, [2] on all.
+// Read with muon_tc_trace_read.
 #ifdef MUON_TC_TRACE
 constexpr int kTraceCtas = 160, kTraceTiles = 96;
-__device__ long long g_tc_trace[3][kTraceCtas][kTraceTiles][4];
-__device__ long long g_tc_life[3][kTraceCtas][2];
-#define TC_TRACE(k, slot)                                                                                       \
-  do {                                                                                                          \
-    const int kind_ = kGram ? (p.g[0].prev ? 1 : 0) : 2;                                                         \
-    if (blockIdx.x < kTraceCtas && (k) < kTraceTiles) g_tc_trace[kind_][blockIdx.x][(k)][(slot)] = clock64();   \
+__device__ long long g_tc_trace[4][kTraceCtas][kTraceTiles][4];
+__device__ long long g_tc_life[4][kTraceCtas][2];
+__device__ long long g_tc_epi[4][kTraceCtas][4];
+__device__ long long g_tc_mma[4][kTraceCtas][4];
+#define TC_KIND (kGram ? (p.g[0].prev ? 1 : 0) : (p.apply ? 3 : 2))
+#define TC_TRACE(k, slot)                                                                          \
+  do {                                                                                             \
+    if (blockIdx.x < kTraceCtas && (k) < kTraceTiles) g_tc_trace[TC_KIND][blockIdx.x][(k)][(slot)] = clock64(); \
   } while (0)
-#define TC_LIFE(slot)                                                                  \
-  do {                                                                                 \
-    const int kind_ = kGram ? (p.g[0].prev ? 1 : 0) : 2;                                \
-    if (blockIdx.x < kTraceCtas) g_tc_life[kind_][blockIdx.x][(slot)] = clock64();      \
+#define TC_LIFE(slot)                                                              \
+  do {                                                                             \
+    if (blockIdx.x < kTraceCtas) g_tc_life[TC_KIND][blockIdx.x][(slot)] = clock64(); \
+  } while (0)
+#define TC_EPI_T0(v) const long long v = clock64()
+#define TC_EPI_ADD(ec, slot, v)                                                                     \
+  do {                                                                                              \
+    if ((ec).quarter == 0 && (ec).slice == 0 && (ec).lane == 0 && (blockIdx.x & 1) == 0 &&          \
+        blockIdx.x < kTraceCtas)                                                                    \
+      g_tc_epi[p.apply ? 3 : 2][blockIdx.x][(slot)] += clock64() - (v);                             \
+  } while (0)
+#define TC_MMA_ADD(kb, v)                 \
+  do {                                    \
+    const long long d_ = clock64() - (v); \
+    if ((kb) == 0) tc_mw[0] += d_;        \
+    if ((kb) < 4) tc_mw[1] += d_;         \
+    tc_mw[2] += d_;                       \
   } while (0)
 #else
 #define TC_TRACE(k, slot)
 #define TC_LIFE(slot)
+#define TC_EPI_T0(v)
+#define TC_EPI_ADD(ec, slot, v)
+#define TC_MMA_ADD(kb, v)
 #endif
 
 // Flattened tile t -> (group, matrix, row block, column block).  Gram tiles
@@ -298,6 +323,9 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true, issued = false;
+#ifdef MUON_TC_TRACE
+  long long tc_mw[3] = {0, 0, 0};
+#endif
   int lt = 0;   // local tile count (trace)
   (void)lt;
   for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits, ++lt) {
@@ -314,11 +342,13 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
     const uint32_t d = tmem_base + (uint32_t)(acc * TN);
     for (int kb = 0; kb < nk; ++kb) {
       TC_PROF_T0(t_f);
+      TC_EPI_T0(t_fw);
       if (!wait_role<false>(&full[stage], phase, abort, p.status, kStatusTimeoutMma)) {
         ok = false;
         break;
       }
       TC_PROF_ADD(1, t_f);
+      TC_MMA_ADD(kb, t_fw);
       ptx::tc_fence_after();
       const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
       const uint32_t sb = sa + A_BYTES;
@@ -350,6 +380,10 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
+#ifdef MUON_TC_TRACE
+  if (blockIdx.x < kTraceCtas)
+    for (int q = 0; q < 3; ++q) g_tc_mma[TC_KIND][blockIdx.x][q] = tc_mw[q];
+#endif
   if (!ok && issued) {
     if (kPair) ptx::umma_commit_pair_mc(drain, 0x1);
     else ptx::umma_commit(drain);
@@ -724,9 +758,11 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   const int lane = ec.lane;
   const int b = k & 1;
   const int c0 = col0 + kGC * gemm_chunk_col(ec, k);
+  TC_EPI_T0(t_x);
   if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
                               kWaitLimitNs))
     return false;
+  TC_EPI_ADD(ec, 0, t_x);
   ec.xphase ^= 1u << b;
   const uint8_t* xh = gemm_in(ec, b);
   const uint8_t* xl = xh + kXBox;
@@ -763,8 +799,10 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   // the inputs were consumed above; once every lane is past this point the
   // input buffer can be refilled
   if (lane == 0) {
+    TC_EPI_T0(t_w);
     if (ec.out_bufs == 2) ptx::bulk_wait_read_1();
     else ptx::bulk_wait_read_all();
+    TC_EPI_ADD(ec, 1, t_w);
   }
   __syncwarp();
   if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 2 * kGC * ec.nslices, r0);
@@ -1075,19 +1113,26 @@ int launch_gemm_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool p
 }  // namespace muon
 
 #ifdef MUON_TC_TRACE
-// Trace reader of -DMUON_TC_TRACE builds: copies g_tc_trace then g_tc_life
-// into dst (bytes >= their sizes) and clears both.
+// Trace reader of -DMUON_TC_TRACE builds: copies g_tc_trace, g_tc_life,
+// g_tc_epi and g_tc_mma, in that order, into dst (bytes >= their sizes) and
+// clears them.
 extern "C" int muon_tc_trace_read(void* dst, size_t bytes) {
-  const size_t a = sizeof(muon::g_tc_trace), b = sizeof(muon::g_tc_life);
-  if (bytes < a + b) return -1;
-  if (cudaMemcpyFromSymbol(dst, muon::g_tc_trace, a) != cudaSuccess) return -2;
-  if (cudaMemcpyFromSymbol(static_cast<char*>(dst) + a, muon::g_tc_life, b) != cudaSuccess) return -3;
-  void* pa = nullptr;
-  void* pb = nullptr;
-  if (cudaGetSymbolAddress(&pa, muon::g_tc_trace) != cudaSuccess) return -4;
-  if (cudaGetSymbolAddress(&pb, muon::g_tc_life) != cudaSuccess) return -4;
-  cudaMemset(pa, 0, a);
-  cudaMemset(pb, 0, b);
+  struct Part { const void* sym; size_t size; };
+  const Part parts[4] = {{&muon::g_tc_trace, sizeof(muon::g_tc_trace)},
+                         {&muon::g_tc_life, sizeof(muon::g_tc_life)},
+                         {&muon::g_tc_epi, sizeof(muon::g_tc_epi)},
+                         {&muon::g_tc_mma, sizeof(muon::g_tc_mma)}};
+  size_t total = 0;
+  for (const Part& q : parts) total += q.size;
+  if (bytes < total) return -1;
+  size_t off = 0;
+  for (const Part& q : parts) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, q.sym) != cudaSuccess) return -2;
+    if (cudaMemcpy(static_cast<char*>(dst) + off, addr, q.size, cudaMemcpyDeviceToHost) != cudaSuccess) return -3;
+    if (cudaMemset(addr, 0, q.size) != cudaSuccess) return -4;
+    off += q.size;
+  }
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
 }
 #endif
