@@ -165,3 +165,83 @@ def test_rank_deficient_gradient():
     assert s[2] > 0.1 and s[3] < 1e-2 * s[0]
     res = oracle_for(W, G, torch.zeros_like(G), 1e-3)
     assert np.linalg.norm(Oo[0].numpy() - res.O) / np.linalg.norm(res.O) < 2e-2
+
+
+def test_workspace_errors_leave_state_untouched():
+    """NULL, misaligned or short workspaces are refused before any launch:
+    MUON_ERR_WORKSPACE with a message, W and M unchanged; the exact size runs."""
+    Ws, Gs, Ms, lrs = _inputs("experts_4x256x1024", steady=True)
+    dev = torch.device("cuda", 0)
+    Wd, Gd, Md = [w.to(dev) for w in Ws], [g.to(dev) for g in Gs], [m.to(dev) for m in Ms]
+    ms = B.MuonStep(0)
+    descs, n = ms.descs_from_tensors(Wd, Gd, Md, lrs)
+    need = ms.workspace_bytes(descs, n)
+    ws = torch.empty(need + 512, dtype=torch.uint8, device=dev)
+    base = ws.data_ptr()
+    assert base % 256 == 0
+    s = torch.cuda.current_stream(dev).cuda_stream
+    for ptr, nbytes, msg in ((0, need, "NULL"), (base + 16, need, "256-byte aligned"), (base, need - 1, "too small")):
+        assert B.muon_step(ms.h, descs, n, ptr, nbytes, s) == B.MUON_ERR_WORKSPACE
+        assert msg in B.muon_last_error_message(ms.h)
+    torch.cuda.synchronize(dev)
+    for i in range(len(Ws)):
+        assert torch.equal(Wd[i].cpu().view(torch.int16), Ws[i].view(torch.int16))
+        assert torch.equal(Md[i].cpu(), Ms[i])
+    assert B.muon_step(ms.h, descs, n, base, need, s) == B.MUON_OK
+    torch.cuda.synchronize(dev)
+    assert B.muon_check_status(ms.h, base, s) == B.MUON_OK
+    ms.close()
+
+
+def _device_copies(batch, dev):
+    Ws, Gs, Ms, lrs = batch
+    return ([w.to(dev) for w in Ws], [g.to(dev) for g in Gs], [m.to(dev) for m in Ms], lrs,
+            [torch.empty(w.shape, dtype=torch.float32, device=dev) for w in Ws])
+
+
+def _assert_same(dev_out, ref):
+    Wd, _, Md, _, Od = dev_out
+    for i in range(len(Wd)):
+        assert torch.equal(Wd[i].cpu().float(), ref[0][i].float())
+        assert torch.equal(Md[i].cpu(), ref[1][i])
+        assert torch.equal(Od[i].cpu(), ref[2][i])
+
+
+def test_one_handle_many_batches_and_streams():
+    """One handle steps differently shaped batches in turn on a side stream,
+    and two handles step on two streams at once: every result equals a fresh
+    handle's on the default stream, bit for bit."""
+    dev = torch.device("cuda", 0)
+    A = _inputs("experts_4x256x1024", steady=True)
+    Bt = _inputs("odd_shapes", steady=True)
+    ref_a, ref_b = run_gpu(*A), run_gpu(*Bt)
+    side = torch.cuda.Stream(dev)
+    ms = B.MuonStep(0)
+    for batch, ref in ((A, ref_a), (Bt, ref_b), (A, ref_a)):
+        d = _device_copies(batch, dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            ms.step(d[0], d[1], d[2], d[3], d[4], stream=side.cuda_stream)
+        side.synchronize()
+        assert ms.check_status(stream=side.cuda_stream) == B.MUON_OK
+        _assert_same(d, ref)
+    ms.close()
+    h1, h2 = B.MuonStep(0), B.MuonStep(0)
+    da, db = _device_copies(A, dev), _device_copies(Bt, dev)
+    for h, d in ((h1, da), (h2, db)):
+        descs, n = h.descs_from_tensors(d[0], d[1], d[2], d[3], d[4])
+        h.workspace(h.workspace_bytes(descs, n))
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for s in (s1, s2):
+        s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s1):
+        h1.step(da[0], da[1], da[2], da[3], da[4], stream=s1.cuda_stream)
+    with torch.cuda.stream(s2):
+        h2.step(db[0], db[1], db[2], db[3], db[4], stream=s2.cuda_stream)
+    torch.cuda.synchronize(dev)
+    assert h1.check_status(stream=s1.cuda_stream) == B.MUON_OK
+    assert h2.check_status(stream=s2.cuda_stream) == B.MUON_OK
+    _assert_same(da, ref_a)
+    _assert_same(db, ref_b)
+    h1.close()
+    h2.close()
