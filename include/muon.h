@@ -6,7 +6,8 @@
  *
  *   1. M <- beta*M + G                       one fp32 momentum state per
  *      parameter ("Training a 1T-Params MoE on EU public infrastructure",
- *      tanhow.com, optimizer-state paragraph);
+ *      tanhow.com, optimizer-state paragraph); or beta*M + (1 - beta)*G with
+ *      the `dampening` variant;
  *   2. X = M (rows <= cols) or M^T (rows > cols), so that A = X X^T is the
  *      smaller Gram matrix;  X <- X / (||X||_F + eps);
  *   3. `ns_iters` Newton-Schulz iterations (5 per step: "ZAYA1 MoE training on

@@ -20,8 +20,9 @@
 //   kPair = true: a cluster of two CTAs on two SMs computes 256 x 256 tiles
 //       with tcgen05.mma.cta_group::2 (M = 256, N = 256): each CTA loads 128
 //       rows of the left operand and 128 columns of the right one, so a stage
-//       is 32 KiB instead of 48 and six stages fit; the even CTA issues the
-//       MMAs, and the odd CTA's copies complete on the even CTA's barriers.
+//       is 32 KiB instead of 48 and six (Gram) or five (GEMM, whose epilogue
+//       staging is larger) stages fit; the even CTA issues the MMAs, and the
+//       odd CTA's copies complete on the even CTA's barriers.
 //
 // Tiles of all matrices of a launch form one flattened list walked with a
 // static stride (deterministic; one launch per phase covers the whole ragged
@@ -30,6 +31,13 @@
 // epilogue warps drain the other accumulator through swizzled shared-memory
 // staging with TMA loads and stores, so the epilogue of tile t overlaps the
 // MMAs of tile t + 1.
+//
+// In the last iteration the GEMM applies the weight update instead of storing
+// X': each matrix's W arrives by TMA with its X tile (tensor maps the momentum
+// kernel publishes in the workspace) and leaves updated the same way.
+//
+// Every launch waits for its predecessor on the stream (griddepcontrol) after
+// its set-up, so it can be launched as a programmatic dependent.
 //
 // Every wait is bounded (one second): on a time-out the kernel records the
 // role in the status word, lets its copies and MMAs in flight finish, frees
