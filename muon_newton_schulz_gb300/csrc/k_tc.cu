@@ -172,11 +172,11 @@ __device__ long long g_tc_mma[4][kTraceCtas][4];
     if (blockIdx.x < kTraceCtas) g_tc_life[TC_KIND][blockIdx.x][(slot)] = clock64(); \
   } while (0)
 #define TC_EPI_T0(v) const long long v = clock64()
-#define TC_EPI_ADD(ec, slot, v)                                                                     \
+#define TC_EPI_ADD(ec, kind, slot, v)                                                               \
   do {                                                                                              \
     if ((ec).quarter == 0 && (ec).slice == 0 && (ec).lane == 0 && (blockIdx.x & 1) == 0 &&          \
         blockIdx.x < kTraceCtas)                                                                    \
-      g_tc_epi[p.apply ? 3 : 2][blockIdx.x][(slot)] += clock64() - (v);                             \
+      g_tc_epi[(kind)][blockIdx.x][(slot)] += clock64() - (v);                                      \
   } while (0)
 #define TC_MMA_ADD(kb, v)                 \
   do {                                    \
@@ -189,7 +189,7 @@ __device__ long long g_tc_mma[4][kTraceCtas][4];
 #define TC_TRACE(k, slot)
 #define TC_LIFE(slot)
 #define TC_EPI_T0(v)
-#define TC_EPI_ADD(ec, slot, v)
+#define TC_EPI_ADD(ec, kind, slot, v)
 #define TC_MMA_ADD(kb, v)
 #endif
 
@@ -540,8 +540,10 @@ __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, con
   uint8_t* tr = ro + 2048;
   const int lane = ec.lane;
   if (lane == 0) {   // the stores that last read this buffer are done with it
+    TC_EPI_T0(t_w);
     if (single) ptx::bulk_wait_read_all();
     else ptx::bulk_wait_read_1();
+    TC_EPI_ADD(ec, single ? 1 : 0, 1, t_w);
   }
   __syncwarp();
 #pragma unroll
@@ -601,9 +603,11 @@ __device__ __forceinline__ bool gram_chunk(const PhaseParams& p, const PhaseGrou
   float pa[32];
   if (G.prev) {
     const int b = k & 1;
+    TC_EPI_T0(t_x);
     if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
                                 kWaitLimitNs))
       return false;
+    TC_EPI_ADD(ec, G.prev ? 1 : 0, 0, t_x);
     ec.xphase ^= 1u << b;
     const uint8_t* pb = ec.buf + 4096 + 2048 * b;
 #pragma unroll
@@ -626,7 +630,11 @@ __device__ __forceinline__ bool gram_tile_epilogue(const PhaseParams& p, const P
   if (gc.count <= 0) return true;
   uint32_t va[32], vb[32];
   ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * gc.first), va);
-  ptx::tmem_ld_wait_regs(va);
+  {
+    TC_EPI_T0(t_m);
+    ptx::tmem_ld_wait_regs(va);
+    TC_EPI_ADD(ec, G.prev ? 1 : 0, 2, t_m);
+  }
 #pragma unroll 1
   for (int k = 0; k < gc.count; k += 2) {
     const bool has1 = k + 1 < gc.count;
@@ -770,7 +778,7 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   if (!ptx::mbar_wait_bounded(&ec.xfull[b], (ec.xphase >> b) & 1u, abort, p.status, kStatusTimeoutEpilogue,
                               kWaitLimitNs))
     return false;
-  TC_EPI_ADD(ec, 0, t_x);
+  TC_EPI_ADD(ec, p.apply ? 3 : 2, 0, t_x);
   ec.xphase ^= 1u << b;
   const uint8_t* xh = gemm_in(ec, b);
   const uint8_t* xl = xh + kXBox;
@@ -810,7 +818,7 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
     TC_EPI_T0(t_w);
     if (ec.out_bufs == 2) ptx::bulk_wait_read_1();
     else ptx::bulk_wait_read_all();
-    TC_EPI_ADD(ec, 1, t_w);
+    TC_EPI_ADD(ec, p.apply ? 3 : 2, 1, t_w);
   }
   __syncwarp();
   if (k + 2 < cnt) gemm_prefetch(p, G, tl, ec, b, c0 + 2 * kGC * ec.nslices, r0);
