@@ -685,9 +685,10 @@ __device__ __forceinline__ void gemm_prefetch(const PhaseParams& p, const PhaseG
   if (ec.lane == 0) {
     const ApplyEntry* ae = p.apply ? &p.apply[G.first + tl.mat] : nullptr;
     const uint32_t wbytes = ae ? (ae->d.w_bf16 ? 32u * kGC * 2u : 32u * kGC * 4u) : 0u;
-    ptx::mbar_arrive_expect_tx(&ec.xfull[b], 2 * kXBox + wbytes);
+    ptx::mbar_arrive_expect_tx(&ec.xfull[b], (p.x_lo_in ? 2 : 1) * kXBox + wbytes);
     ptx::tma_load_4d(gemm_in(ec, b), &p.map_c[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
-    ptx::tma_load_4d(gemm_in(ec, b) + kXBox, &p.map_d[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
+    if (p.x_lo_in)
+      ptx::tma_load_4d(gemm_in(ec, b) + kXBox, &p.map_d[tl.g], c0, r0, tl.mat, G.buf_in, &ec.xfull[b]);
     if (ae) {
       if (ae->d.tall) ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, r0, c0, &ec.xfull[b]);
       else ptx::tma_load_2d(gemm_out(ec, b), &ae->wmap, c0, r0, &ec.xfull[b]);
@@ -783,13 +784,23 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   const uint8_t* xh = gemm_in(ec, b);
   const uint8_t* xl = xh + kXBox;
   float f[kGC];
+  if (p.x_lo_in) {
 #pragma unroll
-  for (int i = 0; i < kGC / 8; ++i) {
-    float hv[8], lv[8];
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(xh + sw_off(lane, i, kXRowBytes)), hv);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(xl + sw_off(lane, i, kXRowBytes)), lv);
+    for (int i = 0; i < kGC / 8; ++i) {
+      float hv[8], lv[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(xh + sw_off(lane, i, kXRowBytes)), hv);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(xl + sw_off(lane, i, kXRowBytes)), lv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) f[8 * i + j] = s * fmaf(ar, hv[j] + lv[j], __uint_as_float(v[8 * i + j]));
+      for (int j = 0; j < 8; ++j) f[8 * i + j] = s * fmaf(ar, hv[j] + lv[j], __uint_as_float(v[8 * i + j]));
+    }
+  } else {   // X stored as bf16 alone (the last stored iterates)
+#pragma unroll
+    for (int i = 0; i < kGC / 8; ++i) {
+      float hv[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(xh + sw_off(lane, i, kXRowBytes)), hv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[8 * i + j] = s * fmaf(ar, hv[j], __uint_as_float(v[8 * i + j]));
+    }
   }
   if (p.apply) {
     // last iteration: update the W tile that came with this X tile and store
@@ -825,6 +836,7 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
   const int o = ec.out_bufs == 2 ? ec.obuf : 0;
   uint8_t* oh = gemm_out(ec, o);
   uint8_t* ol = oh + kXBox;
+  const bool lo_out = p.x_lo_out != 0;
 #pragma unroll
   for (int i = 0; i < kGC / 8; ++i) {
     uint32_t hw[4], lw[4];
@@ -837,13 +849,14 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
       lw[j] = *reinterpret_cast<const uint32_t*>(&l2);
     }
     *reinterpret_cast<uint4*>(oh + sw_off(lane, i, kXRowBytes)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(ol + sw_off(lane, i, kXRowBytes)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    if (lo_out)
+      *reinterpret_cast<uint4*>(ol + sw_off(lane, i, kXRowBytes)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
   ptx::fence_async_smem();
   __syncwarp();
   if (lane == 0 && r0 < G.m) {  // a box that starts past the last row is not stored
     ptx::tma_store_4d(&p.map_c[tl.g], oh, c0, r0, tl.mat, G.buf_out);
-    ptx::tma_store_4d(&p.map_d[tl.g], ol, c0, r0, tl.mat, G.buf_out);
+    if (lo_out) ptx::tma_store_4d(&p.map_d[tl.g], ol, c0, r0, tl.mat, G.buf_out);
   }
   if (lane == 0) ptx::bulk_commit();   // one group per chunk (possibly empty)
   ec.obuf ^= 1;

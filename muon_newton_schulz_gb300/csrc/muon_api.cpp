@@ -637,6 +637,11 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
 
   // ---- Newton-Schulz iterations
   const int grid = h->sm_count;
+  // tensor-core mode stores X_t as the bf16 pair (hi, lo) for t < lo_iters and
+  // as bf16 alone for the last MUON_X_LO_TAIL stored iterates, whose rounding
+  // the remaining iterations amplify least (X0, written by the momentum
+  // kernel, always has both halves)
+  const int lo_iters = std::max(1, iters - MUON_X_LO_TAIL);
   for (int it = 0; it < iters; ++it) {
     const int cur = it % 2, nxt = 1 - cur;
     for (int phase = 0; phase < 3; ++phase) {
@@ -650,6 +655,8 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
         // failure-path test hook (environment, read per step): the step's
         // first Gram launch withholds its loads so its bounded waits expire
         pp->withhold_loads = (withhold && it == 0 && phase == 0 && gb == 0) ? 1 : 0;
+        pp->x_lo_in = (phase == 2 && it < lo_iters) ? 1 : 0;
+        pp->x_lo_out = (phase == 2 && it + 1 < lo_iters) ? 1 : 0;
         pp->scale = (it == 0 && phase != 1) ? scale : nullptr;
         pp->coef_acc = phase == 1 ? cfg.c : 1.f;
         pp->coef_prev = phase == 1 ? cfg.b : (phase == 2 ? cfg.a : 0.f);

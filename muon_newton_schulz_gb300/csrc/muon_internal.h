@@ -125,6 +125,8 @@ struct PhaseParams {
   uint32_t* status;        // kernel status word (bounded waits)
   const ApplyEntry* apply; // last GEMM: apply W -= lr_eff * X' instead of storing X' (or null)
   int32_t withhold_loads;  // test hook: the producer issues no loads, so the waits run out
+  int32_t x_lo_in;         // GEMM: the input X has its lo half (else X = hi)
+  int32_t x_lo_out;        // GEMM: store the lo half of X' (else X' = hi only)
 };
 
 // Handle accessors for the allocation-free entry point (defined in muon_api.cpp).
@@ -165,6 +167,12 @@ constexpr int kTcK = 64;
 #endif
 constexpr int kGemmChunk = MUON_GEMM_CHUNK;
 static_assert(kGemmChunk == 16 || kGemmChunk == 32, "GEMM epilogue chunk of 16 or 32 columns");
+
+// Stored Newton-Schulz iterates, counted from the last, that keep only the
+// bf16 hi half of X (tensor-core mode).
+#ifndef MUON_X_LO_TAIL
+#define MUON_X_LO_TAIL 1
+#endif
 
 // The Newton-Schulz phases run on CTA pairs (256 x 256 tiles) unless built
 // with -DMUON_USE_PAIR=0 (single CTAs, 128 x 256 tiles).
