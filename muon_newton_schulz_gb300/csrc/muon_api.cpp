@@ -260,8 +260,8 @@ bool encode_map(muon_handle h, CUtensorMap* map, void* base, uint64_t d0, uint64
 }
 
 // 2-D map of a caller's weight matrix whose box is one GEMM epilogue chunk:
-// 16 columns x 32 rows (wide), 32 columns x 16 rows (tall: W is X^T), with
-// the swizzle matching the box row (32 B..128 B).
+// kGemmChunk columns x 32 rows (wide), 32 columns x kGemmChunk rows (tall: W
+// is X^T), with the swizzle matching the box row (32 B..128 B).
 bool encode_w_map(muon_handle h, CUtensorMap* map, const muon_matrix_desc& d, bool tall) {
   const bool bf = d.w_dtype == MUON_BF16;
   const uint64_t es = bf ? 2 : 4;
