@@ -41,8 +41,11 @@ Pins (tests/test_oracle_pins.py): the singular-value polynomial closed form
 via SVD, convergence to the polar factor with (1.5, -0.5, 0) against
 scipy.linalg.polar, exact symmetry, scale / transpose / orthogonal
 equivariance, rank preservation, the momentum closed form, brute-force
-triple-loop products, exact rational values of the scalar polynomial, and
-torch's fp32->bf16 cast for ``round_to_bf16``.  Every function here has a pin.
+triple-loop products, exact rational values of the scalar polynomial,
+torch's fp32->bf16 cast for ``round_to_bf16``, and for ``nesterov_input`` a
+two-step case with orthogonal gradient rows whose update has a closed form
+(singular values beta^2 and 1 + beta), evaluated in 50-digit decimal
+arithmetic.  Every function here has a pin.
 """
 from __future__ import annotations
 
@@ -84,6 +87,18 @@ def momentum(M: np.ndarray, G: np.ndarray, beta: float, dampening: bool = False)
         g = (1.0 - float(beta)) * g
     out = float(beta) * M.astype(np.float64) + g
     return out.astype(np.float32)
+
+
+def nesterov_input(M_new: np.ndarray, G: np.ndarray, beta: float, dampening: bool = False) -> np.ndarray:
+    """Step 1b, only with ``nesterov`` (reading R3): the Newton-Schulz input
+    looks one momentum step ahead, ``G + beta*M_new`` with the momentum just
+    updated in step 1, evaluated in fp64 from the stored fp32 values.  With
+    ``dampening`` (reading R17) the gradient term is ``(1 - beta)*G`` as in
+    the momentum itself."""
+    g = G.astype(np.float64)
+    if dampening:
+        g = (1.0 - float(beta)) * g
+    return g + float(beta) * M_new.astype(np.float64)
 
 
 def orient(M: np.ndarray) -> tuple[np.ndarray, bool]:
@@ -175,10 +190,7 @@ def muon_step_matrix(W: np.ndarray, G: np.ndarray, M: np.ndarray, lr: float,
     """Steps 1-6 for one matrix.  ``W`` is float32 (holding bf16 values when
     ``w_is_bf16``), ``G`` and ``M`` float32, all rows x cols."""
     M_new = momentum(M, G, cfg.beta, cfg.dampening)
-    src = M_new
-    if cfg.nesterov:
-        gin = (1.0 - float(cfg.beta)) * G.astype(np.float64) if cfg.dampening else G.astype(np.float64)
-        src = gin + float(cfg.beta) * M_new.astype(np.float64)
+    src = nesterov_input(M_new, G, cfg.beta, cfg.dampening) if cfg.nesterov else M_new
     X, transposed = orient(src)
     X0 = frobenius_normalise(X, cfg.eps)
     Xk = newton_schulz(X0, cfg.a, cfg.b, cfg.c, cfg.ns_iters)

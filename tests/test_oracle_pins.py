@@ -421,25 +421,124 @@ def test_dampened_momentum_is_a_single_rounding():
         assert got[i] == best
 
 
-def test_dampened_nesterov_input():
-    """Dampening and Nesterov together: the NS input is (1 - beta) G + beta M_new;
-    from a zero momentum that is (1 - beta)(1 + beta) G up to the fp32 rounding
-    of the stored M_new = fl((1 - beta) G), a positive multiple of G, so the
-    update equals the plain one (eps = 0) to about fp32 precision."""
+def test_dampened_nesterov_from_zero_momentum_is_a_rescaling():
+    """Dampening and Nesterov together from a zero momentum: the NS input is a
+    positive multiple of G up to the fp32 rounding of the stored momentum, so
+    the update equals the plain one (eps = 0) to about fp32 precision."""
     G = _rng(65).standard_normal((6, 10)).astype(np.float32)
     Z = np.zeros_like(G)
     plain = O.muon_step_matrix(Z, G, Z, 0.0, O.OracleConfig(eps=0.0))
     both = O.muon_step_matrix(Z, G, Z, 0.0, O.OracleConfig(eps=0.0, nesterov=True, dampening=True))
     assert _rel(both.O, plain.O) < 1e-6
-    # a dropped (1 - beta) on the gradient term would still be a multiple of G
-    # here, so the non-zero-momentum check below is the one that pins the form
-    M = _rng(66).standard_normal((6, 10)).astype(np.float32)
-    a = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig(dampening=True))
-    b = O.muon_step_matrix(Z, G, M, 0.0, O.OracleConfig(dampening=True, nesterov=True))
-    beta = float(np.float32(0.95))
-    # the dampened momentum itself, and the Nesterov input built from it
-    assert np.array_equal(a.M, O.momentum(M, G, beta, dampening=True))
-    src = (1.0 - beta) * G.astype(np.float64) + beta * a.M.astype(np.float64)
-    X0 = O.frobenius_normalise(src, 1e-7)
-    want = O.newton_schulz(X0, O.NS_A, O.NS_B, O.NS_C, 5)
-    assert _rel(b.O, want) < 1e-12
+
+
+# --- the Nesterov input, pinned by a two-step case with a closed-form answer --------
+#
+# G1 has one non-zero row u (row 0) and G2 one non-zero row v (row 1), with u and
+# v orthogonal unit vectors whose entries are +-1/2, so every stored fp32 value
+# below is exact.  From M0 = 0, two steps give M2 = beta*G1 + G2 (plain form) and
+# the Nesterov input G2 + beta*M2 = beta^2 G1 + (1 + beta) G2: its rows are
+# orthogonal, so its singular values are beta^2 and 1 + beta, with u and v as
+# right singular vectors.  Newton-Schulz maps each normalised singular value
+# s -> p(s) = a s + b s^3 + c s^5, so the update is
+#     O = [p^5(beta^2 / F) u ; p^5((1 + beta) / F) v],   F = sqrt(beta^4 + (1 + beta)^2),
+# evaluated here in 50-digit decimal arithmetic, independently of numpy.
+
+U_ROW = np.array([0.5, 0.5, 0.5, 0.5])
+V_ROW = np.array([0.5, -0.5, 0.5, -0.5])
+
+
+def _two_step_O(cfg):
+    G1 = np.zeros((2, 4), np.float32)
+    G1[0] = U_ROW
+    G2 = np.zeros((2, 4), np.float32)
+    G2[1] = V_ROW
+    Z = np.zeros((2, 4), np.float32)
+    first = O.muon_step_matrix(Z, G1, Z, 0.0, cfg)
+    second = O.muon_step_matrix(Z, G2, first.M, 0.0, cfg)
+    return second.O
+
+
+def _decimal_update(row_norms):
+    """[p^5(n0 / F) u ; p^5(n1 / F) v] for the singular values n0, n1 given as
+    Decimals (F their 2-norm), as float64."""
+    import decimal
+    with decimal.localcontext() as ctx:
+        ctx.prec = 50
+        D = decimal.Decimal
+        a, b, c = D(str(A)), D(str(B)), D(str(C))
+        n0, n1 = row_norms
+        F = (n0 * n0 + n1 * n1).sqrt()
+        out = []
+        for n in (n0, n1):
+            s = n / F
+            for _ in range(5):
+                s = a * s + b * s ** 3 + c * s ** 5
+            out.append(float(s))
+    return np.stack([out[0] * U_ROW, out[1] * V_ROW])
+
+
+def _beta_decimal():
+    import decimal
+    return decimal.Decimal(float(np.float32(0.95)))
+
+
+def test_nesterov_input_two_step_closed_form():
+    import decimal
+    beta = _beta_decimal()
+    want = _decimal_update((beta * beta, 1 + beta))
+    got = _two_step_O(O.OracleConfig(eps=0.0, nesterov=True))
+    assert np.abs(got - want).max() < 1e-12
+    # the plain step sees M2 itself, with singular values beta and 1
+    plain = _two_step_O(O.OracleConfig(eps=0.0))
+    assert np.abs(plain - _decimal_update((beta, decimal.Decimal(1)))).max() < 1e-12
+    assert np.abs(got - plain).max() > 1e-3
+
+
+def test_dampened_nesterov_input_two_step_closed_form():
+    """With dampening, M1 = (1 - beta) G1 and M2 = beta M1 + (1 - beta) G2,
+    stored in fp32: row 0 of M2 is fl32(beta (1 - beta)) u (beta (1 - beta)
+    has 44 significant bits, so the stored state is rounded once), row 1 is
+    (1 - beta) v.  The Nesterov input (1 - beta) G2 + beta M2 then has
+    singular values beta fl32(beta (1 - beta)) and (1 - beta)(1 + beta)."""
+    import decimal
+    beta = _beta_decimal()
+    d = 1 - beta                                   # exact in fp32 (Sterbenz)
+    stored = decimal.Decimal(float(np.float32(float(beta * d))))   # fp32 storage of the momentum
+    want = _decimal_update((beta * stored, d * (1 + beta)))
+    got = _two_step_O(O.OracleConfig(eps=0.0, nesterov=True, dampening=True))
+    assert np.abs(got - want).max() < 1e-12
+
+
+def _nesterov_mutants():
+    def swapped(M_new, G, beta, dampening=False):     # M_new + beta*G instead of G + beta*M_new
+        g = G.astype(np.float64)
+        if dampening:
+            g = (1.0 - float(beta)) * g
+        return M_new.astype(np.float64) + float(beta) * g
+
+    def ignored(M_new, G, beta, dampening=False):     # no look-ahead at all
+        return M_new.astype(np.float64)
+
+    def undampened_gradient(M_new, G, beta, dampening=False):   # (1 - beta) dropped from G
+        return G.astype(np.float64) + float(beta) * M_new.astype(np.float64)
+
+    return [swapped, ignored, undampened_gradient]
+
+
+@pytest.mark.parametrize("mutant", _nesterov_mutants(), ids=lambda f: f.__name__)
+@pytest.mark.parametrize("dampening", [False, True])
+def test_planted_nesterov_mistakes_fail_the_two_step_pin(mutant, dampening, monkeypatch):
+    import decimal
+    beta = _beta_decimal()
+    if dampening:
+        d = 1 - beta
+        stored = decimal.Decimal(float(np.float32(float(beta * d))))
+        want = _decimal_update((beta * stored, d * (1 + beta)))
+    else:
+        if mutant.__name__ == "undampened_gradient":
+            pytest.skip("identical to the correct form without dampening")
+        want = _decimal_update((beta * beta, 1 + beta))
+    monkeypatch.setattr(O, "nesterov_input", mutant)
+    got = _two_step_O(O.OracleConfig(eps=0.0, nesterov=True, dampening=dampening))
+    assert not (np.abs(got - want).max() < 1e-6)
