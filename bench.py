@@ -91,17 +91,30 @@ def measured_traffic(workload: str):
     return None
 
 
+# A timed window at least this long runs the GPU into its power cap the way
+# the sustained bf16 measurement (4 s of back-to-back GEMMs) does; a shorter
+# one is compared with the burst measurement.
+SUSTAINED_WINDOW_S = 2.0
+
+
 def peaks():
-    """(bf16 burst TF/s, bf16 sustained TF/s, HBM GB/s, kind).  The kernels
-    are timed inside a long run of back-to-back steps, under the power cap, so
-    the sustained figure is the roofline's denominator; the burst one is
-    reported beside it."""
+    """(bf16 burst TF/s, bf16 sustained TF/s, HBM GB/s, kind)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         burst = float(d["bf16_tflops"])
         return burst, float(d.get("bf16_tflops_sustained", burst)), float(d["hbm_gbs"]), "measured"
     return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def roofline_peak(window_s: float, burst_tf: float, sustained_tf: float, kind: str):
+    """(peak TF/s, description) for a timed window of `window_s` seconds: the
+    sustained figure from SUSTAINED_WINDOW_S on, the burst one below it."""
+    sustained = window_s >= SUSTAINED_WINDOW_S
+    peak = sustained_tf if sustained else burst_tf
+    desc = (f"{kind} bf16 {'sustained' if sustained else 'burst'} "
+            f"(timed window {window_s:.2f} s; sustained from {SUSTAINED_WINDOW_S:.0f} s)")
+    return peak, desc
 
 
 class ClockSampler:
@@ -189,6 +202,57 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_min_mhz": min(x[1] for x in sel),
                 "sm_max_mhz": max(x[2] for x in sel), "power_w_median": statistics.median(x[3] for x in sel),
                 "reasons": reasons, "samples": len(sel), "period_ms": self.period_ms}
+
+
+def link_rates(host, dev, reps: int = 3):
+    """(H2D GB/s, D2H GB/s): best of `reps` copies of one pinned host tensor
+    to the device and back, with CUDA events on the current stream."""
+    import torch
+    d = torch.empty(host.shape, dtype=host.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = host.numel() * host.element_size()
+    out = []
+    for direction in ("h2d", "d2h"):
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if direction == "h2d":
+                d.copy_(host, non_blocking=True)
+            else:
+                host.copy_(d, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+        out.append(nbytes / (best / 1e3) / 1e9)
+    return out[0], out[1]
+
+
+def numa_placement(ptr: int):
+    """NUMA nodes holding the pages of the mapping that contains `ptr`
+    (/proc/self/numa_maps), e.g. "N0=16384", or None."""
+    try:
+        best = None
+        for line in open("/proc/self/numa_maps"):
+            start = int(line.split(" ", 1)[0], 16)
+            if start <= ptr and (best is None or start > best[0]):
+                best = (start, line)
+        if best is None:
+            return None
+        return " ".join(t for t in best[1].split() if t.startswith("N") and "=" in t) or None
+    except Exception:
+        return None
+
+
+def gpu_numa_node(dev_index: int):
+    """NUMA node of the GPU's PCI function from sysfs, or None."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev_index)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        return int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read().strip())
+    except Exception:
+        return None
 
 
 def oracle_baseline(workload, n_matrices: int, steps: int, warmup: int):
@@ -339,7 +403,9 @@ def run_gb300(args):
     value = total_mats / (ms_step / 1e3)
     sym_flops = wl.workload_flops(w)
     dense_flops = wl.workload_flops(w, symmetric=False)
-    burst_tf, peak_tf, hbm_gbs, peak_kind = peaks()
+    burst_tf, sustained_tf, hbm_gbs, peak_kind = peaks()
+    # the roofline's denominator follows the regime of the timed window
+    peak_tf, peak_desc = roofline_peak(ms_total / 1e3, burst_tf, sustained_tf, peak_kind)
 
     # dominant kernel: the GEMM with the a X epilogue (61% of the flops)
     gemm_flops = sum(2.0 * min(r, c) ** 2 * max(r, c) for r, c in w.shapes)
@@ -362,9 +428,9 @@ def run_gb300(args):
         if phase["apply"]["launches_per_step"] > 0:
             phase["apply"]["gbs"] = k5_bytes / (phase["apply"]["ms_per_step"] / 1e3) / 1e9
 
-    # end to end with the state in pinned host memory: every step copies G,
-    # W, M in and W, M out, pipelined in chunks of whole matrices against the
-    # steps of other chunks (muon_newton_schulz_gb300.offload)
+    # end to end with the state in pinned host memory, through the library's
+    # muon_step_host: every step copies G, W, M in and W, M out, chunks of
+    # whole matrices pipelined against the steps of other chunks
     e2e = None
     if not args.no_e2e:
         from muon_newton_schulz_gb300.offload import HostOffloadedMuon
@@ -373,8 +439,10 @@ def run_gb300(args):
         Mh = [x.cpu().pin_memory() for x in Ms]
         h2d = sum(x.numel() * x.element_size() for x in Wh + Gh + Mh)
         d2h = sum(x.numel() * x.element_size() for x in Wh + Mh)
+        h2d_gbs, d2h_gbs = link_rates(Gh[0], dev)
         off = HostOffloadedMuon(local, chunk=args.e2e_chunk, slots=args.e2e_slots, mode=mode)
-        off.step(Wh, Gh, Mh, lrs)           # warm-up: allocates the slot buffers
+        for _ in range(2):
+            off.step(Wh, Gh, Mh, lrs)       # warm-up: allocates the staging slots, builds the plans
         torch.cuda.synchronize(dev)
         barrier()
         t0 = time.perf_counter()
@@ -382,15 +450,24 @@ def run_gb300(args):
             off.step(Wh, Gh, Mh, lrs)
         torch.cuda.synchronize(dev)
         dt = (time.perf_counter() - t0) / args.e2e_steps
+        if off.check_status() != B.MUON_OK:
+            raise RuntimeError("kernel status not OK after the end-to-end steps")
         off.close()
         if world > 1:
             import torch.distributed as dist
             t = torch.tensor([dt], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             dt = float(t.item())
+        # the link bounds the step from below by the slower direction's bytes
+        link_ms = max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9)) * 1e3
         e2e = {"value": total_mats / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": dt * 1e3,
-               "pipeline": f"chunks of {args.e2e_chunk} matrices, {args.e2e_slots} device slots"}
+               "api": "muon_step_host (C ABI): W, G, M in pinned host memory",
+               "pipeline": f"chunks of {args.e2e_chunk} matrices, {args.e2e_slots} device slots",
+               "link_h2d_gbs": h2d_gbs, "link_d2h_gbs": d2h_gbs, "link_bound_ms_per_step": link_ms,
+               "frac_of_link_bound": link_ms / (dt * 1e3),
+               "host_pages_numa": numa_placement(Gh[0].data_ptr()), "gpu_numa_node": gpu_numa_node(local),
+               "host_cpus": len(os.sched_getaffinity(0))}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -411,12 +488,14 @@ def run_gb300(args):
         "tflops_dense_equivalent": dense_flops / (ms_step / 1e3) / 1e12 * world,
         "frac_of_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / peak_tf,
         "frac_of_burst_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / burst_tf,
+        "frac_of_sustained_peak_symmetric": sym_flops / (ms_step / 1e3) / 1e12 / sustained_tf,
         "roofline": {"kernel": "k_ns_tc_pair<GEMM> (gemm_update)", "bound": "tensor", "achieved": achieved,
-                     "peak": peak_tf, "peak_kind": f"{peak_kind} bf16 sustained (timed inside back-to-back steps, "
-                                                   f"under the power cap)",
-                     "burst_peak": burst_tf, "unit": "TFLOP/s",
+                     "peak": peak_tf, "peak_kind": peak_desc,
+                     "burst_peak": burst_tf, "sustained_peak": sustained_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf if achieved is not None else None,
-                     "frac_of_burst": achieved / burst_tf if achieved is not None else None, "traffic": traffic,
+                     "frac_of_burst": achieved / burst_tf if achieved is not None else None,
+                     "frac_of_sustained": achieved / sustained_tf if achieved is not None else None,
+                     "traffic": traffic,
                      "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": gemm_ms},
         "phases": phase,
         "e2e": e2e,

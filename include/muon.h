@@ -128,15 +128,25 @@ muon_status muon_create(const muon_config* cfg, int device, muon_handle* out);
 muon_status muon_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n, size_t* bytes);
 
 /* One Muon step over `n` matrices.  `ws` is device memory of at least
- * muon_workspace_size() bytes, 256-byte aligned, used only by this call while
- * it runs on `stream` (its contents need not be preserved between calls).
- * n == 0 launches nothing and returns MUON_OK. */
+ * muon_workspace_size() bytes, 256-byte aligned, that overlaps none of the
+ * descriptors' buffers (MUON_ERR_INVALID_ARG otherwise), used only by this
+ * call while it runs on `stream` (its contents need not be preserved between
+ * calls).  n == 0 launches nothing and returns MUON_OK.
+ *
+ * The handle keeps the plans of its most recent batches (up to 8): a call
+ * whose descriptor array is byte-for-byte one seen before, with the same
+ * workspace pointer, skips validation and planning and launches the kernels
+ * with the parameter blocks and TMA tensor maps built then (they depend on
+ * nothing else: the configuration is fixed per handle). */
 muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n,
                       void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, then reads and clears the kernels' status word in
  * `ws`: MUON_ERR_TIMEOUT if a kernel of an earlier step gave up a bounded
- * wait, else MUON_OK (or MUON_ERR_CUDA if the stream reports an error). */
+ * wait, else MUON_OK (or MUON_ERR_CUDA if the stream reports an error).
+ * ws == NULL reads and clears the status word of muon_step_noalloc's fixed
+ * array on the handle's device.  A step whose wait timed out leaves W
+ * unchanged when the time-out happened before its last kernel started. */
 muon_status muon_check_status(muon_handle h, void* ws, void* stream);
 
 muon_status muon_destroy(muon_handle h);
@@ -156,6 +166,53 @@ muon_status muon_read_profile(muon_handle h, muon_phase_stats* out);
 
 /* Number of kernel launches this handle has issued since it was created. */
 int64_t muon_launch_count(muon_handle h);
+
+/* Number of step plans this handle has built (validation, tile lists, tensor
+ * maps); a batch repeated with the same descriptors and workspace reuses its
+ * plan and does not add to it. */
+int64_t muon_plan_builds(muon_handle h);
+
+/* ---- Steps on buffers in host memory ------------------------------------
+ *
+ * The optimizer state may live in host memory when HBM is short: the pages
+ * keep activations in Grace memory and move them over NVLink-C2C ("Training a
+ * 1T-Params MoE on EU public infrastructure", tanhow.com, activation-offload
+ * paragraph).  muon_step_host runs the step on descriptors whose W, G, M or
+ * O_out (as selected by `host_buffers`) are host pointers: it copies chunks
+ * of whole matrices into device staging slots, runs muon_step on each chunk
+ * and copies W, M and O_out back, with the copies of one chunk overlapping
+ * the step of another (a copy-in, a step and a copy-out stream owned by the
+ * handle, ordered by events; one cudaMemcpy2DAsync per buffer).  Buffers not
+ * selected are device pointers, used in place.  The results equal
+ * muon_step's on the same values bit for bit. */
+#define MUON_HOST_W 1
+#define MUON_HOST_G 2
+#define MUON_HOST_M 4
+#define MUON_HOST_O 8
+
+typedef struct {
+    int32_t host_buffers;     /* MUON_HOST_* bits: which buffers are host pointers */
+    int32_t chunk_matrices;   /* matrices per chunk (>= 1) */
+    int32_t slots;            /* device staging slots in the ring (>= 2) */
+    int32_t reserved;         /* 0 */
+} muon_host_pipeline;
+
+/* Bytes of device workspace muon_step_host needs for this batch and pipeline:
+ * `slots` staging slots, each holding one chunk's host-resident buffers and
+ * the workspace of its muon_step. */
+muon_status muon_host_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n,
+                                     const muon_host_pipeline* pl, size_t* bytes);
+
+/* One Muon step over `n` matrices whose selected buffers are in host memory.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to be asynchronous; they, and the device workspace `ws` (at
+ * least muon_host_workspace_size() bytes, 256-byte aligned), must stay alive
+ * and untouched until `stream` has passed the step: the call only enqueues
+ * work.  The handle's copy and step streams wait for the work already on
+ * `stream`, and `stream` waits for their last copy.  Errors as muon_step; a
+ * descriptor error launches and copies nothing. */
+muon_status muon_step_host(muon_handle h, const muon_matrix_desc* descs, int n,
+                           const muon_host_pipeline* pl, void* ws, size_t ws_bytes, void* stream);
 
 /* Size of the fixed device workspace that muon_step_noalloc uses. */
 #define MUON_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
@@ -178,9 +235,9 @@ int64_t muon_launch_count(muon_handle h);
  * launches nothing.  All calls on a device share the array, which keeps the
  * last call's contents (nothing in it needs to start at zero); calls that
  * overlap on the GPU race on it and must be serialised by the caller.
- * Otherwise identical to muon_step().  The kernels' status word sits inside
- * the fixed array, which callers cannot address, so muon_check_status does
- * not apply to this entry point. */
+ * Otherwise identical to muon_step().  The kernels' status word sits at the
+ * start of the fixed array: muon_check_status(h, NULL, stream) reads and
+ * clears it. */
 muon_status muon_step_noalloc(muon_handle h, const muon_matrix_desc* descs, int n, void* stream);
 
 #ifdef __cplusplus

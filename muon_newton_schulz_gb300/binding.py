@@ -51,6 +51,16 @@ class muon_matrix_desc(ctypes.Structure):
     ]
 
 
+MUON_HOST_W = 1
+MUON_HOST_G = 2
+MUON_HOST_M = 4
+MUON_HOST_O = 8
+
+
+class muon_host_pipeline(ctypes.Structure):
+    _fields_ = [("host_buffers", c_int32), ("chunk_matrices", c_int32), ("slots", c_int32), ("reserved", c_int32)]
+
+
 class muon_phase_stats(ctypes.Structure):
     _fields_ = [
         ("ms", c_double * MUON_NUM_PHASES),
@@ -101,6 +111,14 @@ def load_library(build_if_missing: bool = False):
     lib.muon_read_profile.argtypes = [H, POINTER(muon_phase_stats)]
     lib.muon_launch_count.argtypes = [H]
     lib.muon_launch_count.restype = c_int64
+    lib.muon_plan_builds.argtypes = [H]
+    lib.muon_plan_builds.restype = c_int64
+    lib.muon_host_workspace_size.argtypes = [H, POINTER(muon_matrix_desc), c_int, POINTER(muon_host_pipeline),
+                                             POINTER(c_size_t)]
+    lib.muon_host_workspace_size.restype = c_int
+    lib.muon_step_host.argtypes = [H, POINTER(muon_matrix_desc), c_int, POINTER(muon_host_pipeline), c_void_p,
+                                   c_size_t, c_void_p]
+    lib.muon_step_host.restype = c_int
     lib.muon_step_noalloc.argtypes = [H, POINTER(muon_matrix_desc), c_int, c_void_p]
     lib.muon_step_noalloc.restype = c_int
     for name in ("muon_create", "muon_workspace_size", "muon_step", "muon_check_status", "muon_destroy",
@@ -142,8 +160,9 @@ def muon_step_noalloc(h, descs, n: int, stream: int) -> int:
 MUON_STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 
-def muon_check_status(h, ws: int, stream: int) -> int:
-    return load_library().muon_check_status(h, c_void_p(ws), c_void_p(stream))
+def muon_check_status(h, ws, stream: int) -> int:
+    """ws None reads the status word of muon_step_noalloc's fixed array."""
+    return load_library().muon_check_status(h, c_void_p(ws) if ws else None, c_void_p(stream))
 
 
 def muon_destroy(h) -> int:
@@ -170,6 +189,27 @@ def muon_read_profile(h):
 
 def muon_launch_count(h) -> int:
     return int(load_library().muon_launch_count(h))
+
+
+def make_pipeline(host_buffers: int, chunk_matrices: int = 1, slots: int = 3) -> muon_host_pipeline:
+    pl = muon_host_pipeline()
+    pl.host_buffers, pl.chunk_matrices, pl.slots, pl.reserved = int(host_buffers), int(chunk_matrices), int(slots), 0
+    return pl
+
+
+def muon_host_workspace_size(h, descs, n: int, pl: muon_host_pipeline):
+    nbytes = c_size_t(0)
+    st = load_library().muon_host_workspace_size(h, descs, n, byref(pl), byref(nbytes))
+    return st, nbytes.value
+
+
+def muon_step_host(h, descs, n: int, pl: muon_host_pipeline, ws: int, ws_bytes: int, stream: int) -> int:
+    """muon_step on descriptors whose selected buffers are host pointers."""
+    return load_library().muon_step_host(h, descs, n, byref(pl), c_void_p(ws), ws_bytes, c_void_p(stream))
+
+
+def muon_plan_builds(h) -> int:
+    return int(load_library().muon_plan_builds(h))
 
 
 def make_descs(items):
@@ -253,10 +293,16 @@ class MuonStep:
         import torch
         nbytes = self.workspace_bytes(descs, n)
         ws = self.workspace(nbytes)
-        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        cur = torch.cuda.current_stream(self.device).cuda_stream
+        s = stream if stream is not None else cur
         st = muon_step(self.h, descs, n, ws.data_ptr(), ws.numel(), s)
         if st != MUON_OK:
             raise MuonError(st, muon_last_error_message(self.h))
+        if s != cur:
+            # the workspace belongs to the stream it was allocated on: tell the
+            # caching allocator it is also in use on `s`, so that a later
+            # replacement does not hand the old block out while `s` still runs
+            ws.record_stream(torch.cuda.ExternalStream(s, device=torch.device("cuda", self.device)))
         return st
 
     def step(self, Ws, Gs, Ms, lrs, Os=None, stream=None):

@@ -414,6 +414,7 @@ struct EpiCtx {
   int nslices;
   int out_bufs;        // GEMM output staging buffers (1 or 2)
   int lane;
+  bool skip_w;         // last GEMM: an earlier launch of the step timed out, leave W as it is
 };
 
 // ---------------------------------------------------------------- Gram epilogue
@@ -812,7 +813,7 @@ __device__ __forceinline__ bool gemm_chunk(const PhaseParams& p, const PhaseGrou
     ptx::fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (r0 < G.m) {
+      if (r0 < G.m && !ec.skip_w) {
         if (ae->d.tall) ptx::tma_store_2d(&ae->wmap, ws, r0, c0);
         else ptx::tma_store_2d(&ae->wmap, ws, c0, r0);
       }
@@ -1057,6 +1058,9 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
     ec.nslices = C::kSlices;
     ec.out_bufs = C::kOutBufs;
     ec.lane = lane;
+    // the earlier kernels of the step have completed (grid dependency wait
+    // above): a time-out among them leaves its bit in the status word
+    ec.skip_w = !kGram && p.apply && p.status && *reinterpret_cast<volatile uint32_t*>(p.status) != 0u;
     run_epilogue<kGram, kPair>(p, pi, tfull, tempty, tmem_base, ec, abort);
   }
 

@@ -7,11 +7,13 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <new>
 #include <string>
 #include <utility>
@@ -37,6 +39,29 @@ struct StepEvents {
   int apply_launches = 0;
 };
 
+// One entry of a step's launch sequence: a kernel with its parameter block
+// (an index into StepPlan::elt or StepPlan::phase), or a profiling mark.
+struct LaunchRec {
+  enum Kind : uint8_t { kMomentum, kFinalize, kGram, kGemm, kApply, kMark } kind;
+  uint32_t index;
+  bool pdl;
+};
+
+// Everything muon_step launches for one batch: validated once, then reused
+// while the caller passes the same descriptors (byte for byte) and workspace.
+struct StepPlan {
+  std::vector<muon_matrix_desc> key;
+  const void* ws = nullptr;
+  size_t need = 0;
+  std::vector<muon::EltParams> elt;
+  std::vector<muon::PhaseParams> phase;
+  std::vector<LaunchRec> seq;
+  int iters = 0;
+  int apply_launches = 0;
+};
+
+constexpr size_t kPlanCacheEntries = 32;
+
 }  // namespace
 
 struct muon_handle_s {
@@ -49,6 +74,21 @@ struct muon_handle_s {
   bool profiling = false;
   std::vector<StepEvents> recorded;
   std::vector<cudaEvent_t> pool;
+  // failure-path test hook, read once at muon_create: the first Gram launch of
+  // every step issues no loads, so its bounded waits run out
+  bool withhold_loads = false;
+  // most recently used step plans first
+  std::vector<std::unique_ptr<StepPlan>> plans;
+  int64_t plan_builds = 0;
+  // muon_step_host: copy-in, step and copy-out streams and their events,
+  // created on first use
+  cudaStream_t host_streams[3] = {nullptr, nullptr, nullptr};
+  std::vector<cudaEvent_t> host_events;
+  // the workspace of the last muon_step_host call: a status word at the start
+  // of each of its slots
+  const void* host_ws = nullptr;
+  size_t host_slot_bytes = 0;
+  int host_slots = 0;
 };
 
 namespace {
@@ -104,10 +144,12 @@ muon_status check_config(const muon_config& c, std::string& why) {
 
 struct Range { uintptr_t lo, hi; int desc; const char* what; };
 
-muon_status validate(const muon_matrix_desc* d, int n, std::string& why) {
+// Checks every descriptor; on success `ranges` holds the byte range of each
+// caller buffer (sorted by address, none overlapping).
+muon_status validate(const muon_matrix_desc* d, int n, std::string& why, std::vector<Range>& ranges) {
+  ranges.clear();
   if (n < 0) { why = "n must be >= 0"; return MUON_ERR_INVALID_ARG; }
   if (n > 0 && !d) { why = "descs is NULL"; return MUON_ERR_INVALID_ARG; }
-  std::vector<Range> ranges;
   for (int i = 0; i < n; ++i) {
     const muon_matrix_desc& x = d[i];
     const std::string at = "desc " + std::to_string(i) + ": ";
@@ -341,183 +383,30 @@ cudaEvent_t take_event(muon_handle h) {
   return e;
 }
 
-}  // namespace
-
-extern "C" {
-
-void muon_config_default(muon_config* c) {
-  if (!c) return;
-  c->beta = 0.95f;
-  c->a = 3.4445f;
-  c->b = -4.7750f;
-  c->c = 2.0315f;
-  c->eps = 1e-7f;
-  c->scale_coeff = 0.2f;
-  c->ns_iters = 5;
-  c->nesterov = 0;
-  c->dampening = 0;
-  c->mode = MUON_MODE_BF16;
-}
-
-const char* muon_status_string(muon_status s) {
-  switch (s) {
-    case MUON_OK: return "MUON_OK";
-    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
-    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
-    case MUON_ERR_WORKSPACE: return "MUON_ERR_WORKSPACE";
-    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
-    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+// Cached plan for exactly these descriptors and this workspace, moved to the
+// front of the cache, or null.
+const StepPlan* find_plan(muon_handle h, const muon_matrix_desc* descs, int n, const void* ws) {
+  if (n <= 0 || !descs) return nullptr;
+  for (size_t i = 0; i < h->plans.size(); ++i) {
+    const StepPlan& p = *h->plans[i];
+    if (p.ws != ws || p.key.size() != (size_t)n) continue;
+    if (std::memcmp(p.key.data(), descs, sizeof(muon_matrix_desc) * (size_t)n) != 0) continue;
+    if (i > 0) std::rotate(h->plans.begin(), h->plans.begin() + i, h->plans.begin() + i + 1);
+    return h->plans.front().get();
   }
-  return "MUON_ERR_UNKNOWN";
+  return nullptr;
 }
 
-muon_status muon_create(const muon_config* cfg, int device, muon_handle* out) {
-  if (!out) return MUON_ERR_INVALID_ARG;
-  *out = nullptr;
-  muon_config c;
-  if (cfg) c = *cfg; else muon_config_default(&c);
-  std::string why;
-  muon_status st = check_config(c, why);
-  if (st != MUON_OK) return st;
-  if (device < -1) return MUON_ERR_INVALID_ARG;
-  muon_handle h = new (std::nothrow) muon_handle_s();
-  if (!h) return MUON_ERR_CUDA;
-  h->cfg = c;
-  if (device >= 0) {
-    int count = 0;
-    if (cudaGetDeviceCount(&count) != cudaSuccess || device >= count) {
-      cudaGetLastError();
-      delete h;
-      return MUON_ERR_UNSUPPORTED;
-    }
-    int major = 0, minor = 0, sms = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    // kernels are built for sm_103a, whose tcgen05 features are not forward compatible
-    if (major != 10 || minor != 3) {
-      delete h;
-      return MUON_ERR_UNSUPPORTED;
-    }
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn) {
-      cudaGetLastError();
-      delete h;
-      return MUON_ERR_CUDA;
-    }
-    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    h->device = device;
-    h->sm_count = sms;
-  }
-  *out = h;
-  return MUON_OK;
-}
-
-muon_status muon_destroy(muon_handle h) {
-  if (!h) return MUON_ERR_INVALID_ARG;
-  if (h->device >= 0) {
-    DeviceGuard g(h->device);
-    for (auto& s : h->recorded)
-      for (cudaEvent_t e : s.ev) cudaEventDestroy(e);
-    for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
-  }
-  delete h;
-  return MUON_OK;
-}
-
-const char* muon_last_error_message(muon_handle h) { return h ? h->err.c_str() : ""; }
-
-int64_t muon_launch_count(muon_handle h) { return h ? h->launches : 0; }
-
-muon_status muon_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n, size_t* bytes) {
-  if (!h || !bytes) return MUON_ERR_INVALID_ARG;
-  h->err.clear();
-  std::string why;
-  muon_status st = validate(descs, n, why);
-  if (st != MUON_OK) return fail(h, st, why);
-  Plan P = build_plan(h->cfg, descs, n);
-  *bytes = P.mats.empty() ? 0 : P.bytes;
-  return MUON_OK;
-}
-
-muon_status muon_set_profiling(muon_handle h, int enable) {
-  if (!h) return MUON_ERR_INVALID_ARG;
-  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
-  h->profiling = enable != 0;
-  return MUON_OK;
-}
-
-muon_status muon_read_profile(muon_handle h, muon_phase_stats* out) {
-  if (!h || !out) return MUON_ERR_INVALID_ARG;
-  std::memset(out, 0, sizeof(*out));
-  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
-  DeviceGuard guard(h->device);
-  muon_status st = MUON_OK;
-  for (StepEvents& s : h->recorded) {
-    const std::vector<cudaEvent_t>& e = s.ev;
-    if (cudaEventSynchronize(e.back()) != cudaSuccess) {
-      st = fail(h, MUON_ERR_CUDA, std::string("cudaEventSynchronize: ") + cudaGetErrorString(cudaGetLastError()));
-      break;
-    }
-    float t = 0.f;
-    // e[0] start, e[1] after momentum+norm, then 3 per iteration, then after apply
-    cudaEventElapsedTime(&t, e[0], e[1]);
-    out->ms[0] += t;
-    out->launches[0] += 2;
-    for (int it = 0; it < s.iters; ++it) {
-      for (int k = 0; k < 3; ++k) {
-        cudaEventElapsedTime(&t, e[1 + 3 * it + k], e[2 + 3 * it + k]);
-        out->ms[1 + k] += t;
-        out->launches[1 + k] += 1;
-      }
-    }
-    cudaEventElapsedTime(&t, e[e.size() - 2], e[e.size() - 1]);
-    out->ms[4] += t;
-    out->launches[4] += s.apply_launches;
-    out->steps += 1;
-  }
-  for (StepEvents& s : h->recorded)
-    for (cudaEvent_t e : s.ev) h->pool.push_back(e);
-  h->recorded.clear();
-  return st;
-}
-
-muon_status muon_check_status(muon_handle h, void* ws, void* stream) {
-  if (!h) return MUON_ERR_INVALID_ARG;
-  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
-  if (!ws) return fail(h, MUON_ERR_WORKSPACE, "workspace is NULL");
-  DeviceGuard guard(h->device);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t word = 0;
-  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(word), s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return fail(h, MUON_ERR_CUDA, std::string("muon_check_status: ") + cudaGetErrorString(e));
-  if (word != 0) return fail(h, MUON_ERR_TIMEOUT, "a kernel gave up a bounded wait, status bits " + std::to_string(word));
-  return MUON_OK;
-}
-
-muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void* ws, size_t ws_bytes, void* stream) {
-  if (!h) return MUON_ERR_INVALID_ARG;
-  h->err.clear();
-  std::string why;
-  muon_status st = validate(descs, n, why);
-  if (st != MUON_OK) return fail(h, st, why);
-  Plan P = build_plan(h->cfg, descs, n);
-  if (P.mats.empty()) return MUON_OK;  // nothing to launch
-  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle: create it with a device to run steps");
-  if (!ws) return fail(h, MUON_ERR_WORKSPACE, "workspace is NULL");
-  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(h, MUON_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  if (ws_bytes < P.bytes)
-    return fail(h, MUON_ERR_WORKSPACE, "workspace too small: need " + std::to_string(P.bytes) + " bytes");
-
-  DeviceGuard guard(h->device);
+// Builds every parameter block of one step (elementwise launches, the
+// Newton-Schulz phase launches with their tensor maps) and the launch order.
+muon_status make_plan(muon_handle h, const Plan& P, const muon_matrix_desc* descs, int n, void* ws, StepPlan& out) {
   const muon_config& cfg = h->cfg;
   const bool bf16 = cfg.mode == MUON_MODE_BF16;
   const int iters = cfg.ns_iters;
+  out.key.assign(descs, descs + n);
+  out.ws = ws;
+  out.need = P.bytes;
+  out.iters = iters;
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint32_t* status = reinterpret_cast<uint32_t*>(base + P.off_status);
   float* scale = reinterpret_cast<float*>(base + P.off_scale);
@@ -525,26 +414,8 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   // tensor-core mode applies the weight update in the last GEMM's epilogue,
   // reading each matrix's W from a table the momentum kernel fills
   const bool fused_apply = bf16 && iters > 0;
-  const char* withhold_env = std::getenv("MUON_GB300_TEST_WITHHOLD_LOADS");
-  const bool withhold = bf16 && withhold_env && withhold_env[0] == '1';
+  const bool withhold = bf16 && h->withhold_loads;
   muon::ApplyEntry* apply_table = reinterpret_cast<muon::ApplyEntry*>(base + P.off_apply);
-
-  StepEvents se;
-  auto mark = [&]() {
-    if (!h->profiling || (int)h->recorded.size() >= kMaxProfiledSteps) return;
-    cudaEvent_t e = take_event(h);
-    if (e) {
-      cudaEventRecord(e, reinterpret_cast<cudaStream_t>(stream));
-      se.ev.push_back(e);
-    }
-  };
-  auto launched = [&](int rc, const char* what) -> muon_status {
-    if (rc != 0) {
-      return fail(h, MUON_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString((cudaError_t)rc));
-    }
-    h->launches += 1;
-    return MUON_OK;
-  };
 
   // X of matrix k of a group, ping-pong buffer `buf`: fp32 in validation
   // mode; the bf16 pair (hi, lo) in tensor-core mode
@@ -612,31 +483,26 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
     return true;
   };
 
-  EltParams* ep = new (std::nothrow) EltParams;
-  PhaseParams* pp = new (std::nothrow) PhaseParams;
-  if (!ep || !pp) {
-    delete ep;
-    delete pp;
-    return fail(h, MUON_ERR_CUDA, "host allocation failed");
-  }
-  struct Free { EltParams* a; PhaseParams* b; ~Free() { delete a; delete b; } } free_guard{ep, pp};
-
   const int final_buf = iters % 2;
   // every launch after the step's first is a programmatic dependent of the
   // kernel before it (the kernels wait for their predecessor themselves)
   bool pdl = false;
-  mark();
+  auto push = [&](LaunchRec::Kind k, uint32_t idx) {
+    out.seq.push_back({k, idx, pdl});
+    if (k != LaunchRec::kMark) pdl = muon::kUsePdl;
+  };
+  push(LaunchRec::kMark, 0);
   for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
     const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
-    if (!fill_elt(*ep, b, e, final_buf)) return MUON_ERR_CUDA;
-    if ((st = launched(muon::launch_momentum_norm(*ep, stream, pdl), "momentum/norm kernel")) != MUON_OK) return st;
-    pdl = muon::kUsePdl;
-    if ((st = launched(muon::launch_norm_finalize(*ep, stream, pdl), "norm finalize kernel")) != MUON_OK) return st;
+    out.elt.emplace_back();
+    if (!fill_elt(out.elt.back(), b, e, final_buf)) return MUON_ERR_CUDA;
+    const uint32_t idx = (uint32_t)(out.elt.size() - 1);
+    push(LaunchRec::kMomentum, idx);
+    push(LaunchRec::kFinalize, idx);
   }
-  mark();
+  push(LaunchRec::kMark, 0);
 
   // ---- Newton-Schulz iterations
-  const int grid = h->sm_count;
   // tensor-core mode stores X_t as the bf16 pair (hi, lo) for t < lo_iters and
   // as bf16 alone for the last MUON_X_LO_TAIL stored iterates, whose rounding
   // the remaining iterations amplify least (X0, written by the momentum
@@ -648,12 +514,14 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
       const bool gram = phase < 2;
       for (size_t gb = 0; gb < P.groups.size(); gb += muon::kMaxGroups) {
         const size_t ge = std::min(P.groups.size(), gb + (size_t)muon::kMaxGroups);
+        out.phase.emplace_back();
+        PhaseParams* pp = &out.phase.back();
         std::memset(pp, 0, sizeof(*pp));
         pp->ngroups = (int32_t)(ge - gb);
         pp->status = status;
         pp->apply = (fused_apply && phase == 2 && it + 1 == iters) ? apply_table : nullptr;
-        // failure-path test hook (environment, read per step): the step's
-        // first Gram launch withholds its loads so its bounded waits expire
+        // failure-path test hook: the step's first Gram launch withholds its
+        // loads so its bounded waits expire
         pp->withhold_loads = (withhold && it == 0 && phase == 0 && gb == 0) ? 1 : 0;
         pp->x_lo_in = (phase == 2 && it < lo_iters) ? 1 : 0;
         pp->x_lo_out = (phase == 2 && it + 1 < lo_iters) ? 1 : 0;
@@ -759,16 +627,9 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
           }
         }
         pp->total_tiles = tiles;
-        int rc;
-        if (bf16 && muon::kUsePair)
-          rc = gram ? muon::launch_gram_tc_pair(*pp, h->sm_count, stream, pdl)
-                    : muon::launch_gemm_tc_pair(*pp, h->sm_count, stream, pdl);
-        else if (bf16)
-          rc = gram ? muon::launch_gram_tc(*pp, grid, stream, pdl) : muon::launch_gemm_tc(*pp, grid, stream, pdl);
-        else rc = gram ? muon::launch_gram_f32(*pp, stream, pdl) : muon::launch_gemm_f32(*pp, stream, pdl);
-        if ((st = launched(rc, gram ? "Gram kernel" : "GEMM kernel")) != MUON_OK) return st;
+        push(gram ? LaunchRec::kGram : LaunchRec::kGemm, (uint32_t)(out.phase.size() - 1));
       }
-      mark();
+      push(LaunchRec::kMark, 0);
     }
   }
 
@@ -776,17 +637,508 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   if (!fused_apply) {
     for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
       const size_t e = std::min(P.mats.size(), b + (size_t)muon::kMaxEltMats);
-      if (!fill_elt(*ep, b, e, final_buf)) return MUON_ERR_CUDA;
-      if ((st = launched(muon::launch_apply(*ep, stream, pdl), "apply kernel")) != MUON_OK) return st;
-      se.apply_launches += 1;
+      out.elt.emplace_back();
+      if (!fill_elt(out.elt.back(), b, e, final_buf)) return MUON_ERR_CUDA;
+      push(LaunchRec::kApply, (uint32_t)(out.elt.size() - 1));
+      out.apply_launches += 1;
     }
   }
-  mark();
+  push(LaunchRec::kMark, 0);
+  return MUON_OK;
+}
+
+// Launches a plan's kernels in order on `stream` (profiling events at its
+// marks when enabled).
+muon_status issue_plan(muon_handle h, const StepPlan& plan, void* stream) {
+  DeviceGuard guard(h->device);
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const bool record = h->profiling && (int)h->recorded.size() < kMaxProfiledSteps;
+  StepEvents se;
+  muon_status st = MUON_OK;
+  for (const LaunchRec& r : plan.seq) {
+    int rc = 0;
+    const char* what = "";
+    switch (r.kind) {
+      case LaunchRec::kMark:
+        if (record) {
+          cudaEvent_t e = take_event(h);
+          if (e) {
+            cudaEventRecord(e, cs);
+            se.ev.push_back(e);
+          }
+        }
+        continue;
+      case LaunchRec::kMomentum:
+        rc = muon::launch_momentum_norm(plan.elt[r.index], stream, r.pdl);
+        what = "momentum/norm kernel";
+        break;
+      case LaunchRec::kFinalize:
+        rc = muon::launch_norm_finalize(plan.elt[r.index], stream, r.pdl);
+        what = "norm finalize kernel";
+        break;
+      case LaunchRec::kApply:
+        rc = muon::launch_apply(plan.elt[r.index], stream, r.pdl);
+        what = "apply kernel";
+        break;
+      case LaunchRec::kGram:
+      case LaunchRec::kGemm: {
+        const bool gram = r.kind == LaunchRec::kGram;
+        const PhaseParams& pp = plan.phase[r.index];
+        if (h->cfg.mode == MUON_MODE_BF16 && muon::kUsePair)
+          rc = gram ? muon::launch_gram_tc_pair(pp, h->sm_count, stream, r.pdl)
+                    : muon::launch_gemm_tc_pair(pp, h->sm_count, stream, r.pdl);
+        else if (h->cfg.mode == MUON_MODE_BF16)
+          rc = gram ? muon::launch_gram_tc(pp, h->sm_count, stream, r.pdl)
+                    : muon::launch_gemm_tc(pp, h->sm_count, stream, r.pdl);
+        else
+          rc = gram ? muon::launch_gram_f32(pp, stream, r.pdl) : muon::launch_gemm_f32(pp, stream, r.pdl);
+        what = gram ? "Gram kernel" : "GEMM kernel";
+        break;
+      }
+    }
+    if (rc != 0) {
+      st = fail(h, MUON_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString((cudaError_t)rc));
+      break;
+    }
+    h->launches += 1;
+  }
   if (!se.ev.empty()) {
-    se.iters = iters;
-    if ((int)se.ev.size() == 3 + 3 * iters) h->recorded.push_back(std::move(se));
+    se.iters = plan.iters;
+    se.apply_launches = plan.apply_launches;
+    if (st == MUON_OK && (int)se.ev.size() == 3 + 3 * plan.iters) h->recorded.push_back(std::move(se));
     else for (cudaEvent_t e : se.ev) h->pool.push_back(e);
   }
+  return st;
+}
+
+// ---- steps on host-resident buffers
+
+constexpr uint32_t kHostBits = MUON_HOST_W | MUON_HOST_G | MUON_HOST_M | MUON_HOST_O;
+
+// Where one chunk of matrices is staged inside a slot of the device workspace.
+struct HostChunk {
+  std::vector<int> mats;                    // caller descriptor indices
+  std::vector<std::array<size_t, 4>> off;   // per matrix: staged W, G, M, O_out (or SIZE_MAX)
+  std::vector<std::array<int64_t, 4>> ld;   // their leading dimensions (elements)
+  size_t ws_off = 0, ws_bytes = 0;          // the chunk's muon_step workspace in the slot
+};
+
+struct HostLayout {
+  std::vector<HostChunk> chunks;
+  size_t slot_bytes = 0;
+};
+
+// Elements per staged row: cols rounded up to 16 bytes.
+int64_t staged_ld(int64_t cols, int64_t es) { return (int64_t)align_up((size_t)(cols * es), 16) / es; }
+
+// Chunks of consecutive non-empty matrices and the slot layout: every slot
+// starts with the step workspace (so its status word is at the slot's first
+// byte), followed by the staged host-resident buffers of its chunk.
+void host_layout(const muon_config& cfg, const muon_matrix_desc* d, int n, const muon_host_pipeline& pl,
+                 HostLayout& L) {
+  std::vector<int> mats;
+  for (int i = 0; i < n; ++i)
+    if (d[i].rows > 0 && d[i].cols > 0) mats.push_back(i);
+  size_t ws_max = 0;
+  for (size_t b = 0; b < mats.size(); b += (size_t)pl.chunk_matrices) {
+    HostChunk c;
+    const size_t e = std::min(mats.size(), b + (size_t)pl.chunk_matrices);
+    std::vector<muon_matrix_desc> shapes;
+    for (size_t k = b; k < e; ++k) {
+      c.mats.push_back(mats[k]);
+      shapes.push_back(d[mats[k]]);
+    }
+    c.ws_off = 0;
+    c.ws_bytes = build_plan(cfg, shapes.data(), (int)shapes.size()).bytes;
+    ws_max = std::max(ws_max, c.ws_bytes);
+    L.chunks.push_back(std::move(c));
+  }
+  const size_t stage0 = align_up(ws_max, 1024);
+  L.slot_bytes = stage0;
+  for (HostChunk& c : L.chunks) {
+    size_t off = stage0;
+    for (int idx : c.mats) {
+      const muon_matrix_desc& x = d[idx];
+      std::array<size_t, 4> o;
+      std::array<int64_t, 4> ld;
+      const int64_t wes = x.w_dtype == MUON_BF16 ? 2 : 4;
+      const int64_t es[4] = {wes, 4, 4, 4};
+      const uint32_t bit[4] = {MUON_HOST_W, MUON_HOST_G, MUON_HOST_M, MUON_HOST_O};
+      const bool present[4] = {true, true, true, x.O_out != nullptr};
+      for (int q = 0; q < 4; ++q) {
+        o[q] = SIZE_MAX;
+        ld[q] = 0;
+        if (!present[q] || !(pl.host_buffers & bit[q])) continue;
+        ld[q] = staged_ld(x.cols, es[q]);
+        o[q] = off;
+        off = align_up(off + (size_t)(x.rows * ld[q] * es[q]), 256);
+      }
+      c.off.push_back(o);
+      c.ld.push_back(ld);
+    }
+    L.slot_bytes = std::max(L.slot_bytes, align_up(off, 1024));
+  }
+}
+
+muon_status check_pipeline(const muon_host_pipeline* pl, std::string& why) {
+  if (!pl) { why = "pipeline is NULL"; return MUON_ERR_INVALID_ARG; }
+  if ((uint32_t)pl->host_buffers & ~kHostBits) { why = "host_buffers has unknown bits"; return MUON_ERR_INVALID_ARG; }
+  if (pl->chunk_matrices < 1) { why = "chunk_matrices must be >= 1"; return MUON_ERR_INVALID_ARG; }
+  if (pl->slots < 2 || pl->slots > 64) { why = "slots must be in [2, 64]"; return MUON_ERR_INVALID_ARG; }
+  if (pl->reserved != 0) { why = "reserved must be 0"; return MUON_ERR_INVALID_ARG; }
+  return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void muon_config_default(muon_config* c) {
+  if (!c) return;
+  c->beta = 0.95f;
+  c->a = 3.4445f;
+  c->b = -4.7750f;
+  c->c = 2.0315f;
+  c->eps = 1e-7f;
+  c->scale_coeff = 0.2f;
+  c->ns_iters = 5;
+  c->nesterov = 0;
+  c->dampening = 0;
+  c->mode = MUON_MODE_BF16;
+}
+
+const char* muon_status_string(muon_status s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_WORKSPACE: return "MUON_ERR_WORKSPACE";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+  }
+  return "MUON_ERR_UNKNOWN";
+}
+
+muon_status muon_create(const muon_config* cfg, int device, muon_handle* out) {
+  if (!out) return MUON_ERR_INVALID_ARG;
+  *out = nullptr;
+  muon_config c;
+  if (cfg) c = *cfg; else muon_config_default(&c);
+  std::string why;
+  muon_status st = check_config(c, why);
+  if (st != MUON_OK) return st;
+  if (device < -1) return MUON_ERR_INVALID_ARG;
+  muon_handle h = new (std::nothrow) muon_handle_s();
+  if (!h) return MUON_ERR_CUDA;
+  h->cfg = c;
+  if (device >= 0) {
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || device >= count) {
+      cudaGetLastError();
+      delete h;
+      return MUON_ERR_UNSUPPORTED;
+    }
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    // kernels are built for sm_103a, whose tcgen05 features are not forward compatible
+    if (major != 10 || minor != 3) {
+      delete h;
+      return MUON_ERR_UNSUPPORTED;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      delete h;
+      return MUON_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    h->device = device;
+    h->sm_count = sms;
+    const char* hook = std::getenv("MUON_GB300_TEST_WITHHOLD_LOADS");
+    h->withhold_loads = hook && hook[0] == '1';
+  }
+  *out = h;
+  return MUON_OK;
+}
+
+muon_status muon_destroy(muon_handle h) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  if (h->device >= 0) {
+    DeviceGuard g(h->device);
+    for (auto& s : h->recorded)
+      for (cudaEvent_t e : s.ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
+    for (cudaEvent_t e : h->host_events) cudaEventDestroy(e);
+    for (cudaStream_t st : h->host_streams)
+      if (st) cudaStreamDestroy(st);
+  }
+  delete h;
+  return MUON_OK;
+}
+
+const char* muon_last_error_message(muon_handle h) { return h ? h->err.c_str() : ""; }
+
+int64_t muon_launch_count(muon_handle h) { return h ? h->launches : 0; }
+
+muon_status muon_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n, size_t* bytes) {
+  if (!h || !bytes) return MUON_ERR_INVALID_ARG;
+  h->err.clear();
+  std::string why;
+  std::vector<Range> ranges;
+  muon_status st = validate(descs, n, why, ranges);
+  if (st != MUON_OK) return fail(h, st, why);
+  Plan P = build_plan(h->cfg, descs, n);
+  *bytes = P.mats.empty() ? 0 : P.bytes;
+  return MUON_OK;
+}
+
+muon_status muon_set_profiling(muon_handle h, int enable) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
+  h->profiling = enable != 0;
+  return MUON_OK;
+}
+
+muon_status muon_read_profile(muon_handle h, muon_phase_stats* out) {
+  if (!h || !out) return MUON_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
+  DeviceGuard guard(h->device);
+  muon_status st = MUON_OK;
+  for (StepEvents& s : h->recorded) {
+    const std::vector<cudaEvent_t>& e = s.ev;
+    if (cudaEventSynchronize(e.back()) != cudaSuccess) {
+      st = fail(h, MUON_ERR_CUDA, std::string("cudaEventSynchronize: ") + cudaGetErrorString(cudaGetLastError()));
+      break;
+    }
+    float t = 0.f;
+    // e[0] start, e[1] after momentum+norm, then 3 per iteration, then after apply
+    cudaEventElapsedTime(&t, e[0], e[1]);
+    out->ms[0] += t;
+    out->launches[0] += 2;
+    for (int it = 0; it < s.iters; ++it) {
+      for (int k = 0; k < 3; ++k) {
+        cudaEventElapsedTime(&t, e[1 + 3 * it + k], e[2 + 3 * it + k]);
+        out->ms[1 + k] += t;
+        out->launches[1 + k] += 1;
+      }
+    }
+    cudaEventElapsedTime(&t, e[e.size() - 2], e[e.size() - 1]);
+    out->ms[4] += t;
+    out->launches[4] += s.apply_launches;
+    out->steps += 1;
+  }
+  for (StepEvents& s : h->recorded)
+    for (cudaEvent_t e : s.ev) h->pool.push_back(e);
+  h->recorded.clear();
+  return st;
+}
+
+muon_status muon_check_status(muon_handle h, void* ws, void* stream) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle");
+  if (!ws) {
+    // the fixed array that muon_step_noalloc uses on this handle's device
+    const cudaError_t e = (cudaError_t)muon::static_workspace(h->device, &ws);
+    if (e != cudaSuccess)
+      return fail(h, MUON_ERR_CUDA, std::string("muon_check_status: fixed workspace: ") + cudaGetErrorString(e));
+  }
+  DeviceGuard guard(h->device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // a muon_step_host workspace holds one status word per staging slot
+  const int words = ws == h->host_ws ? h->host_slots : 1;
+  const size_t stride = ws == h->host_ws ? h->host_slot_bytes : 0;
+  uint32_t word = 0;
+  cudaError_t e = cudaSuccess;
+  for (int k = 0; k < words && e == cudaSuccess; ++k) {
+    uint8_t* at = static_cast<uint8_t*>(ws) + (size_t)k * stride;
+    uint32_t w = 0;
+    e = cudaMemcpyAsync(&w, at, sizeof(w), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(at, 0, sizeof(w), s);
+    word |= w;
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(h, MUON_ERR_CUDA, std::string("muon_check_status: ") + cudaGetErrorString(e));
+  if (word != 0) return fail(h, MUON_ERR_TIMEOUT, "a kernel gave up a bounded wait, status bits " + std::to_string(word));
+  return MUON_OK;
+}
+
+muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void* ws, size_t ws_bytes, void* stream) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  h->err.clear();
+  // a batch seen before (same descriptor bytes, same workspace) reuses its
+  // validated plan, parameter blocks and tensor maps
+  const StepPlan* plan = find_plan(h, descs, n, ws);
+  if (plan) {
+    if (ws_bytes < plan->need)
+      return fail(h, MUON_ERR_WORKSPACE, "workspace too small: need " + std::to_string(plan->need) + " bytes");
+    return issue_plan(h, *plan, stream);
+  }
+  std::string why;
+  std::vector<Range> ranges;
+  muon_status st = validate(descs, n, why, ranges);
+  if (st != MUON_OK) return fail(h, st, why);
+  Plan P = build_plan(h->cfg, descs, n);
+  if (P.mats.empty()) return MUON_OK;  // nothing to launch
+  if (!ws) return fail(h, MUON_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(h, MUON_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < P.bytes)
+    return fail(h, MUON_ERR_WORKSPACE, "workspace too small: need " + std::to_string(P.bytes) + " bytes");
+  {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ws), hi = lo + P.bytes;
+    for (const Range& r : ranges)
+      if (r.lo < hi && lo < r.hi)
+        return fail(h, MUON_ERR_INVALID_ARG,
+                    std::string("workspace overlaps desc ") + std::to_string(r.desc) + " " + r.what);
+  }
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle: create it with a device to run steps");
+  std::unique_ptr<StepPlan> fresh(new (std::nothrow) StepPlan);
+  if (!fresh) return fail(h, MUON_ERR_CUDA, "host allocation failed");
+  if ((st = make_plan(h, P, descs, n, ws, *fresh)) != MUON_OK) return st;
+  h->plan_builds += 1;
+  if (h->plans.size() >= kPlanCacheEntries) h->plans.pop_back();
+  h->plans.insert(h->plans.begin(), std::move(fresh));
+  return issue_plan(h, *h->plans.front(), stream);
+}
+
+int64_t muon_plan_builds(muon_handle h) { return h ? h->plan_builds : 0; }
+
+muon_status muon_host_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n,
+                                     const muon_host_pipeline* pl, size_t* bytes) {
+  if (!h || !bytes) return MUON_ERR_INVALID_ARG;
+  h->err.clear();
+  std::string why;
+  muon_status st = check_pipeline(pl, why);
+  if (st != MUON_OK) return fail(h, st, why);
+  std::vector<Range> ranges;
+  if ((st = validate(descs, n, why, ranges)) != MUON_OK) return fail(h, st, why);
+  HostLayout L;
+  host_layout(h->cfg, descs, n, *pl, L);
+  *bytes = L.chunks.empty() ? 0 : L.slot_bytes * (size_t)std::min<size_t>((size_t)pl->slots, L.chunks.size());
+  return MUON_OK;
+}
+
+muon_status muon_step_host(muon_handle h, const muon_matrix_desc* descs, int n, const muon_host_pipeline* pl,
+                           void* ws, size_t ws_bytes, void* stream) {
+  if (!h) return MUON_ERR_INVALID_ARG;
+  h->err.clear();
+  std::string why;
+  muon_status st = check_pipeline(pl, why);
+  if (st != MUON_OK) return fail(h, st, why);
+  std::vector<Range> ranges;
+  if ((st = validate(descs, n, why, ranges)) != MUON_OK) return fail(h, st, why);
+  HostLayout L;
+  host_layout(h->cfg, descs, n, *pl, L);
+  if (L.chunks.empty()) return MUON_OK;
+  // no more slots than chunks
+  const int S = (int)std::min<size_t>((size_t)pl->slots, L.chunks.size());
+  const size_t need = L.slot_bytes * (size_t)S;
+  if (!ws) return fail(h, MUON_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(h, MUON_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need) return fail(h, MUON_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes");
+  {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ws), hi = lo + need;
+    for (const Range& r : ranges)
+      if (r.lo < hi && lo < r.hi)
+        return fail(h, MUON_ERR_INVALID_ARG,
+                    std::string("workspace overlaps desc ") + std::to_string(r.desc) + " " + r.what);
+  }
+  if (h->device < 0) return fail(h, MUON_ERR_UNSUPPORTED, "host-only handle: create it with a device to run steps");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaSuccess;
+  for (cudaStream_t& hs : h->host_streams)
+    if (!hs && (e = cudaStreamCreateWithFlags(&hs, cudaStreamNonBlocking)) != cudaSuccess)
+      return fail(h, MUON_ERR_CUDA, std::string("cudaStreamCreate: ") + cudaGetErrorString(e));
+  // events: start, done, then per slot: loaded, stepped, free
+  const size_t nev = 2 + 3 * (size_t)S;
+  while (h->host_events.size() < nev) {
+    cudaEvent_t ev = nullptr;
+    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+      return fail(h, MUON_ERR_CUDA, std::string("cudaEventCreate: ") + cudaGetErrorString(e));
+    h->host_events.push_back(ev);
+  }
+  cudaStream_t s_in = h->host_streams[0], s_run = h->host_streams[1], s_out = h->host_streams[2];
+  cudaEvent_t ev_start = h->host_events[0], ev_done = h->host_events[1];
+  auto loaded = [&](int k) { return h->host_events[2 + k]; };
+  auto stepped = [&](int k) { return h->host_events[2 + S + k]; };
+  auto freed = [&](int k) { return h->host_events[2 + 2 * S + k]; };
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  auto ck = [&](cudaError_t r, const char* what) -> bool {
+    if (r == cudaSuccess) return true;
+    e = r;
+    h->err = std::string("muon_step_host: ") + what + ": " + cudaGetErrorString(r);
+    return false;
+  };
+  if (!ck(cudaEventRecord(ev_start, cs), "cudaEventRecord")) return MUON_ERR_CUDA;
+  for (cudaStream_t q : {s_in, s_run, s_out})
+    if (!ck(cudaStreamWaitEvent(q, ev_start, 0), "cudaStreamWaitEvent")) return MUON_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  std::vector<muon_matrix_desc> dd;
+  for (size_t c = 0; c < L.chunks.size(); ++c) {
+    const HostChunk& C = L.chunks[c];
+    const int slot = (int)(c % (size_t)S);
+    uint8_t* sb = base + (size_t)slot * L.slot_bytes;
+    if (c >= (size_t)S && !ck(cudaStreamWaitEvent(s_in, freed(slot), 0), "cudaStreamWaitEvent")) return MUON_ERR_CUDA;
+    dd.clear();
+    for (size_t k = 0; k < C.mats.size(); ++k) {
+      const muon_matrix_desc& x = descs[C.mats[k]];
+      muon_matrix_desc y = x;
+      const int64_t wes = x.w_dtype == MUON_BF16 ? 2 : 4;
+      const size_t rowb[4] = {(size_t)(x.cols * wes), (size_t)x.cols * 4, (size_t)x.cols * 4, (size_t)x.cols * 4};
+      const void* src[4] = {x.W, x.G, x.M, x.O_out};
+      const int64_t sld[4] = {x.ldw, x.ldg, x.ldm, x.ldo};
+      const int64_t es[4] = {wes, 4, 4, 4};
+      void* dst[4] = {nullptr, nullptr, nullptr, nullptr};
+      for (int q = 0; q < 4; ++q) {
+        if (C.off[k][q] == SIZE_MAX) continue;
+        dst[q] = sb + C.off[k][q];
+        // inputs: W, G, M (O_out is written only)
+        if (q < 3 && !ck(cudaMemcpy2DAsync(dst[q], (size_t)(C.ld[k][q] * es[q]), src[q], (size_t)(sld[q] * es[q]),
+                                           rowb[q], (size_t)x.rows, cudaMemcpyHostToDevice, s_in),
+                         "cudaMemcpy2DAsync (in)"))
+          return MUON_ERR_CUDA;
+      }
+      if (dst[0]) { y.W = dst[0]; y.ldw = C.ld[k][0]; }
+      if (dst[1]) { y.G = static_cast<const float*>(dst[1]); y.ldg = C.ld[k][1]; }
+      if (dst[2]) { y.M = static_cast<float*>(dst[2]); y.ldm = C.ld[k][2]; }
+      if (dst[3]) { y.O_out = static_cast<float*>(dst[3]); y.ldo = C.ld[k][3]; }
+      dd.push_back(y);
+    }
+    if (!ck(cudaEventRecord(loaded(slot), s_in), "cudaEventRecord") ||
+        !ck(cudaStreamWaitEvent(s_run, loaded(slot), 0), "cudaStreamWaitEvent"))
+      return MUON_ERR_CUDA;
+    if ((st = muon_step(h, dd.data(), (int)dd.size(), sb + C.ws_off, C.ws_bytes, s_run)) != MUON_OK) return st;
+    if (!ck(cudaEventRecord(stepped(slot), s_run), "cudaEventRecord") ||
+        !ck(cudaStreamWaitEvent(s_out, stepped(slot), 0), "cudaStreamWaitEvent"))
+      return MUON_ERR_CUDA;
+    for (size_t k = 0; k < C.mats.size(); ++k) {
+      const muon_matrix_desc& x = descs[C.mats[k]];
+      const int64_t wes = x.w_dtype == MUON_BF16 ? 2 : 4;
+      // outputs: W, M, O_out
+      const int qs[3] = {0, 2, 3};
+      void* hdst[4] = {x.W, nullptr, x.M, x.O_out};
+      const int64_t hld[4] = {x.ldw, 0, x.ldm, x.ldo};
+      const int64_t es[4] = {wes, 4, 4, 4};
+      for (int q : qs) {
+        if (C.off[k][q] == SIZE_MAX) continue;
+        if (!ck(cudaMemcpy2DAsync(hdst[q], (size_t)(hld[q] * es[q]), sb + C.off[k][q], (size_t)(C.ld[k][q] * es[q]),
+                                  (size_t)(x.cols * es[q]), (size_t)x.rows, cudaMemcpyDeviceToHost, s_out),
+                "cudaMemcpy2DAsync (out)"))
+          return MUON_ERR_CUDA;
+      }
+    }
+    if (!ck(cudaEventRecord(freed(slot), s_out), "cudaEventRecord")) return MUON_ERR_CUDA;
+  }
+  if (!ck(cudaEventRecord(ev_done, s_out), "cudaEventRecord") || !ck(cudaStreamWaitEvent(cs, ev_done, 0), "cudaStreamWaitEvent"))
+    return MUON_ERR_CUDA;
+  h->host_ws = ws;
+  h->host_slot_bytes = L.slot_bytes;
+  h->host_slots = S;
   return MUON_OK;
 }
 

@@ -132,6 +132,9 @@ struct PhaseParams {
 // Handle accessors for the allocation-free entry point (defined in muon_api.cpp).
 int handle_device(::muon_handle_s* h);
 void set_handle_error(::muon_handle_s* h, const std::string& msg);
+// Device address of muon_step_noalloc's fixed array on `device` (defined in
+// muon_noalloc.cu); returns a cudaError_t as int.
+int static_workspace(int device, void** out);
 
 // Launch wrappers (defined in the .cu files).  Each returns the launch's
 // cudaError_t as int.  pdl: launch as a programmatic dependent of the

@@ -18,7 +18,8 @@
 //
 // All calls on a device share the one array and it keeps the previous call's
 // contents.  No part of it needs to start at zero: the step writes every word
-// it reads (its status word is cleared by its first kernel).  Calls that
+// it reads.  The kernels' status word sits at the start of the array;
+// muon_check_status(h, NULL, stream) reads and clears it there.  Calls that
 // overlap on the GPU -- on different streams, or from different host threads
 // -- race on the array and must be serialised by the caller.
 #include "muon.h"
@@ -40,8 +41,14 @@ __device__ __align__(256) unsigned char g_static_workspace[kStaticBytes];
 std::mutex g_mutex;
 void* g_address[kMaxDevices] = {};
 
-// Device address of the array on `device`, looked up once per device.
-cudaError_t static_workspace(int device, void** out) {
+}  // namespace
+
+namespace muon {
+
+// Device address of the array on `device`, looked up once per device (also
+// used by muon_check_status to read the kernels' status word in it).
+int static_workspace(int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return (int)cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_address[device]) {
     *out = g_address[device];
@@ -49,18 +56,18 @@ cudaError_t static_workspace(int device, void** out) {
   }
   int old = -1;
   cudaError_t e = cudaGetDevice(&old);
-  if (e != cudaSuccess) return e;
-  if (old != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+  if (e != cudaSuccess) return (int)e;
+  if (old != device && (e = cudaSetDevice(device)) != cudaSuccess) return (int)e;
   void* ptr = nullptr;
   e = cudaGetSymbolAddress(&ptr, g_static_workspace);
   if (old != device) cudaSetDevice(old);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) return (int)e;
   g_address[device] = ptr;
   *out = ptr;
   return cudaSuccess;
 }
 
-}  // namespace
+}  // namespace muon
 
 extern "C" muon_status muon_step_noalloc(muon_handle h, const muon_matrix_desc* descs, int n, void* stream) {
   if (!h) return MUON_ERR_INVALID_ARG;
@@ -80,7 +87,7 @@ extern "C" muon_status muon_step_noalloc(muon_handle h, const muon_matrix_desc* 
     return MUON_ERR_UNSUPPORTED;
   }
   void* ws = nullptr;
-  const cudaError_t e = static_workspace(device, &ws);
+  const cudaError_t e = (cudaError_t)muon::static_workspace(device, &ws);
   if (e != cudaSuccess) {
     muon::set_handle_error(h, std::string("muon_step_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
     return MUON_ERR_CUDA;

@@ -3,14 +3,13 @@
 The pages keep state off the GPU when HBM is short: activations are
 offloaded to Grace memory over NVLink-C2C ("Training a 1T-Params MoE on EU
 public infrastructure", tanhow.com, activation-offload paragraph).  Here the
-weights, gradients and momentum live in pinned host memory and the step runs
-in chunks of whole matrices through a ring of device slots on three streams:
-copy in (H2D), ``muon_step`` on the chunk, copy out (D2H) of W and M.  The
-copies of one chunk overlap the step of another, so the time approaches the
-larger of the transfer time and the compute time.
-
-Only copies and launches are orchestrated here; the step itself is the
-library's ``muon_step`` (torch provides device memory, streams and events).
+weights, gradients and momentum (any subset of them) live in host memory and
+the library's ``muon_step_host`` runs the step in chunks of whole matrices
+through a ring of device staging slots: copies in, ``muon_step`` on the
+chunk, copies out, on three streams the library owns, so that the copies of
+one chunk overlap the step of another.  This module only builds descriptors
+from torch tensors and owns the device workspace (torch provides memory and
+the stream).
 """
 from __future__ import annotations
 
@@ -20,88 +19,48 @@ from . import binding as B
 
 
 class HostOffloadedMuon:
-    """Pipelined Muon steps over host-resident (pinned) W, G, M lists.
+    """Pipelined Muon steps over host-resident tensors.
 
-    ``chunk`` matrices per slot, ``slots`` device slots in the ring.  The
-    matrices of a call must fit the slot buffers allocated on first use (they
-    are re-allocated when a call needs more)."""
+    ``host_buffers`` selects which of W, G, M (and O, when given) are host
+    tensors (``binding.MUON_HOST_*`` bits; default W, G and M); the others are
+    device tensors used in place.  ``chunk`` matrices per staging slot,
+    ``slots`` slots in the ring."""
 
-    def __init__(self, device: int = 0, chunk: int = 4, slots: int = 3, **cfg):
+    def __init__(self, device: int = 0, chunk: int = 1, slots: int = 3,
+                 host_buffers: int = B.MUON_HOST_W | B.MUON_HOST_G | B.MUON_HOST_M, **cfg):
         self.dev = torch.device("cuda", device)
-        self.chunk = max(1, int(chunk))
-        self.nslots = max(2, int(slots))
-        self.muon = [B.MuonStep(device, **cfg) for _ in range(self.nslots)]
-        self.s_in = torch.cuda.Stream(self.dev)
-        self.s_run = torch.cuda.Stream(self.dev)
-        self.s_out = torch.cuda.Stream(self.dev)
-        self._slots = None
-        self._shapes = None
+        self.muon = B.MuonStep(device, **cfg)
+        self.pl = B.make_pipeline(host_buffers, chunk, slots)
+        self._ws = None
 
     def close(self):
-        for m in self.muon:
-            m.close()
+        self.muon.close()
 
-    def _alloc(self, Wh, Gh, Mh):
-        """Chunk list of this batch; slot state is rebuilt when the batch's
-        shapes change (device buffers are then created on first use)."""
-        n = len(Wh)
-        chunks = [list(range(i, min(n, i + self.chunk))) for i in range(0, n, self.chunk)]
-        key = (tuple((tuple(w.shape), w.dtype) for w in Wh), self.chunk)
-        if self._shapes == key:
-            return chunks
-        self._slots = []
-        for _ in range(self.nslots):
-            self._slots.append({
-                "done": torch.cuda.Event(),     # D2H of the slot's last chunk finished
-                "bufs": {},
-            })
-        self._shapes = key
-        return chunks
+    def workspace_bytes(self, descs, n) -> int:
+        st, nbytes = B.muon_host_workspace_size(self.muon.h, descs, n, self.pl)
+        if st != B.MUON_OK:
+            raise B.MuonError(st, B.muon_last_error_message(self.muon.h))
+        return nbytes
 
-    def _slot_tensors(self, slot, idx, Wh):
-        """Per-slot device tensors keyed by position in the chunk and shape."""
-        out = []
-        for k, i in enumerate(idx):
-            key = (k, tuple(Wh[i].shape), Wh[i].dtype)
-            t = slot["bufs"].get(key)
-            if t is None:
-                shape = tuple(Wh[i].shape)
-                t = (torch.empty(shape, dtype=Wh[i].dtype, device=self.dev),
-                     torch.empty(shape, dtype=torch.float32, device=self.dev),
-                     torch.empty(shape, dtype=torch.float32, device=self.dev))
-                slot["bufs"][key] = t
-            out.append(t)
-        return out
+    def step(self, Ws, Gs, Ms, lrs, Os=None, sync: bool = True):
+        """One step; host tensors among Ws, Ms (and Os) are updated in place.
+        With ``sync`` the call returns once the last copy back has completed."""
+        descs, n = B.MuonStep.descs_from_tensors(Ws, Gs, Ms, lrs, Os)
+        nbytes = self.workspace_bytes(descs, n)
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.dev)
+        stream = torch.cuda.current_stream(self.dev)
+        st = B.muon_step_host(self.muon.h, descs, n, self.pl, self._ws.data_ptr(), self._ws.numel(),
+                              stream.cuda_stream)
+        if st != B.MUON_OK:
+            raise B.MuonError(st, B.muon_last_error_message(self.muon.h))
+        if sync:
+            stream.synchronize()
 
-    def step(self, Wh, Gh, Mh, lrs):
-        """One step; Wh and Mh (pinned host tensors) are updated in place.
-        Returns when the last copy back has completed."""
-        chunks = self._alloc(Wh, Gh, Mh)
-        cur = torch.cuda.current_stream(self.dev)
-        self.s_in.wait_stream(cur)
-        for ci, idx in enumerate(chunks):
-            sl = ci % self.nslots
-            slot = self._slots[sl]
-            dev = self._slot_tensors(slot, idx, Wh)
-            # the slot is free once its previous chunk has been copied out
-            self.s_in.wait_event(slot["done"])
-            with torch.cuda.stream(self.s_in):
-                for (w, g, m), i in zip(dev, idx):
-                    w.copy_(Wh[i], non_blocking=True)
-                    g.copy_(Gh[i], non_blocking=True)
-                    m.copy_(Mh[i], non_blocking=True)
-                loaded = torch.cuda.Event()
-                loaded.record(self.s_in)
-            self.s_run.wait_event(loaded)
-            with torch.cuda.stream(self.s_run):
-                self.muon[sl].step([d[0] for d in dev], [d[1] for d in dev], [d[2] for d in dev],
-                                   [lrs[i] for i in idx], stream=self.s_run.cuda_stream)
-                stepped = torch.cuda.Event()
-                stepped.record(self.s_run)
-            self.s_out.wait_event(stepped)
-            with torch.cuda.stream(self.s_out):
-                for (w, g, m), i in zip(dev, idx):
-                    Wh[i].copy_(w, non_blocking=True)
-                    Mh[i].copy_(m, non_blocking=True)
-                slot["done"].record(self.s_out)
-        self.s_out.synchronize()
+    def check_status(self):
+        """Reads and clears the status words of the last step's chunks (one per
+        staging slot) after synchronising the current stream."""
+        if self._ws is None:
+            return B.MUON_OK
+        stream = torch.cuda.current_stream(self.dev).cuda_stream
+        return B.muon_check_status(self.muon.h, self._ws.data_ptr(), stream)

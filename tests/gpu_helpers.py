@@ -23,6 +23,15 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.cpu().view(torch.int16).numpy().astype(np.int32)
 
 
+def bf16_ordered(t: torch.Tensor) -> np.ndarray:
+    """bf16 bit patterns mapped to integers in the order of the values they
+    hold (+0 and -0 both to 0), so adjacent bf16 numbers differ by one, also
+    across zero."""
+    b = bf16_bits(t)
+    mag = b & 0x7FFF
+    return np.where(b < 0, -mag, mag)
+
+
 def f32_ulps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     """Distance in fp32 units in the last place (same sign assumed)."""
     ia = a.astype(np.float32).view(np.int32).astype(np.int64)
@@ -78,13 +87,48 @@ def check_matrix(W0, G, M0, lr, Wg, Mg, Og, res, tol_o, mode_name=""):
         # mismatches only at near-ties, and never more than one bf16 ulp
         assert mism.mean() <= 1e-3, f"W mismatch fraction {mism.mean():.2e}"
         if mism.any():
-            dif = np.abs(bf16_bits(Wg)[mism] - bf16_bits(torch.from_numpy(want).to(torch.bfloat16))[mism])
+            dif = np.abs(bf16_ordered(Wg)[mism] - bf16_ordered(torch.from_numpy(want).to(torch.bfloat16))[mism])
             assert dif.max() <= 1
     else:
         want = (W0.numpy().astype(np.float64) - float(lr_eff) * Og64).astype(np.float32)
         d = f32_ulps(Wg.numpy(), want)
         assert d.max() <= 1
+    check_w_against_oracle(W0, Wg, Og64, res, lr_eff, mode_name)
     return e
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits; 2^-133 below the
+    normal range)."""
+    e = np.floor(np.log2(np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def check_w_against_oracle(W0, Wg, Og64, res, lr_eff, what=""):
+    """The GPU's W against the oracle's own rounded update res.W.  Both round
+    an update of the same W0, and the unrounded values differ by at most
+    `reach` = lr_eff * |O_gpu - O_oracle| (O agrees to the mode's tolerance)
+    plus the fp32 arithmetic of the kernel, so the rounded values differ by at
+    most reach plus half a unit in the last place of each.  Where reach is
+    below half an ulp (the usual case) they are equal or neighbours."""
+    w0 = W0.float().numpy().astype(np.float64)
+    got = Wg.float().numpy().astype(np.float64)
+    want = res.W.astype(np.float64)
+    o_or = np.asarray(res.O, np.float64)
+    x = w0 - float(lr_eff) * o_or                     # the oracle's update before rounding
+    reach = (float(lr_eff) * np.abs(Og64 - o_or)       # what the O difference moves
+             + 1e-6 * float(lr_eff) * np.abs(o_or)     # lr and scale formed in fp32 vs fp64
+             + 4 * 2.0 ** -24 * np.abs(x))             # the kernel's fp32 fma before the final rounding
+    if W0.dtype == torch.bfloat16:
+        half = 0.5 * (bf16_ulp(got) + bf16_ulp(want))
+        mism = got != want
+        assert mism.mean() <= 5e-2, f"{what} W differs from the oracle's at {mism.mean():.2%} of the elements"
+    else:
+        half = 2.0 ** -24 * (np.abs(got) + np.abs(want))
+    err = np.abs(got - want)
+    bad = err > reach + half
+    assert not bad.any(), (f"{what} W off the oracle's by {err[bad].max():.3e} where the O difference allows "
+                           f"{(reach + half)[bad][np.argmax(err[bad])]:.3e}")
 
 
 def run_and_check(workload_name, mode=B.MUON_MODE_BF16, tol_o=2e-2, ns_iters=5, indices=None, nesterov=False,

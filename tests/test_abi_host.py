@@ -174,3 +174,70 @@ def test_create_without_gpu_is_unsupported(lib):
 def test_profiling_calls_on_host_handle(host_handle):
     assert B.muon_set_profiling(host_handle, True) == B.MUON_ERR_UNSUPPORTED
     assert B.muon_launch_count(host_handle) == 0
+
+
+def test_workspace_overlapping_a_buffer_is_rejected(host_handle):
+    base = 1 << 30
+    d = _desc(base=base)
+    arr, n = B.make_descs([d])
+    st, need = B.muon_workspace_size(host_handle, arr, n)
+    assert st == B.MUON_OK
+    # a workspace that starts inside M (M is at base + 2^25)
+    ws = base + (2 << 24) + 4096
+    assert B.muon_step(host_handle, arr, n, ws, need, 0) == B.MUON_ERR_INVALID_ARG
+    assert "workspace overlaps desc 0 M" in B.muon_last_error_message(host_handle)
+    # one that ends inside W
+    ws = base - need + 256
+    ws -= ws % 256
+    assert B.muon_step(host_handle, arr, n, ws, need, 0) == B.MUON_ERR_INVALID_ARG
+    assert "workspace overlaps desc 0 W" in B.muon_last_error_message(host_handle)
+    # one that ends right where W starts, and a disjoint one, pass validation
+    # (and the host-only handle then refuses to run)
+    assert B.muon_step(host_handle, arr, n, base - need, need, 0) == B.MUON_ERR_UNSUPPORTED
+    assert B.muon_step(host_handle, arr, n, 1 << 34, need, 0) == B.MUON_ERR_UNSUPPORTED
+
+
+def test_plan_counter_on_host_handle(host_handle):
+    # a host-only handle validates but never builds a launch plan
+    arr, n = B.make_descs([_desc()])
+    B.muon_step(host_handle, arr, n, 1 << 32, 1 << 30, 0)
+    assert B.muon_plan_builds(host_handle) == 0
+
+
+def test_host_pipeline_workspace(host_handle):
+    items = [_desc(base=(1 << 30) + k * (1 << 27)) for k in range(5)]
+    arr, n = B.make_descs(items)
+    st, one = B.muon_workspace_size(host_handle, arr, 1)
+    assert st == B.MUON_OK
+    sizes = {}
+    for slots in (2, 3, 4):
+        pl = B.make_pipeline(B.MUON_HOST_W | B.MUON_HOST_G | B.MUON_HOST_M, 1, slots)
+        st, sizes[slots] = B.muon_host_workspace_size(host_handle, arr, n, pl)
+        assert st == B.MUON_OK
+    # one slot per chunk in flight: the step's workspace plus the staged W, G, M
+    slot = sizes[2] // 2
+    assert sizes[3] == 3 * slot and sizes[4] == 4 * slot
+    staged = 256 * 512 * (2 + 4 + 4)
+    assert one + staged <= slot <= one + staged + 4096
+    # no more slots than chunks
+    pl = B.make_pipeline(B.MUON_HOST_G, 5, 4)
+    st, b = B.muon_host_workspace_size(host_handle, arr, n, pl)
+    assert st == B.MUON_OK and b % 1024 == 0 and b >= 5 * 256 * 512 * 4
+
+
+@pytest.mark.parametrize("host, chunk, slots, reserved", [(16, 1, 2, 0), (7, 0, 2, 0), (7, 1, 1, 0), (7, 1, 65, 0),
+                                                          (7, 1, 2, 1)])
+def test_host_pipeline_invalid(host_handle, host, chunk, slots, reserved):
+    arr, n = B.make_descs([_desc()])
+    pl = B.make_pipeline(host, chunk, slots)
+    pl.reserved = reserved
+    assert B.muon_host_workspace_size(host_handle, arr, n, pl)[0] == B.MUON_ERR_INVALID_ARG
+    assert B.muon_step_host(host_handle, arr, n, pl, 1 << 34, 1 << 30, 0) == B.MUON_ERR_INVALID_ARG
+
+
+def test_host_step_on_host_handle_is_unsupported(host_handle):
+    arr, n = B.make_descs([_desc()])
+    pl = B.make_pipeline(B.MUON_HOST_G, 1, 2)
+    st, need = B.muon_host_workspace_size(host_handle, arr, n, pl)
+    assert B.muon_step_host(host_handle, arr, n, pl, 1 << 34, need, 0) == B.MUON_ERR_UNSUPPORTED
+    assert B.muon_step_host(host_handle, arr, n, pl, 1 << 34, need - 256, 0) == B.MUON_ERR_WORKSPACE

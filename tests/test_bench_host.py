@@ -57,13 +57,22 @@ def test_code_hash_ignores_comments_and_whitespace():
     assert bench._code_only(a) != bench._code_only(c)
 
 
-def test_peaks_prefer_the_sustained_figure(tmp_path, monkeypatch):
+def test_peaks_read_the_measured_file(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.peaks()[3] == "fallback"
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
         {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6500.0}))
     burst, sustained, hbm, kind = bench.peaks()
     assert (burst, sustained, hbm, kind) == (1900.0, 1700.0, 6500.0, "measured")
+
+
+def test_roofline_peak_follows_the_timed_window():
+    # a short window (20 steps of about 7 ms) is a burst; seconds of steps run
+    # into the power cap like the sustained measurement
+    peak, desc = bench.roofline_peak(0.135, 1942.5, 1708.6, "measured")
+    assert peak == 1942.5 and "burst" in desc
+    peak, desc = bench.roofline_peak(bench.SUSTAINED_WINDOW_S, 1942.5, 1708.6, "measured")
+    assert peak == 1708.6 and "sustained" in desc
 
 
 def test_traffic_is_reported_only_for_the_captured_code(tmp_path, monkeypatch):

@@ -245,3 +245,39 @@ def test_one_handle_many_batches_and_streams():
     _assert_same(db, ref_b)
     h1.close()
     h2.close()
+
+
+def test_repeated_batch_reuses_its_plan():
+    """A batch stepped again with the same descriptors and workspace reuses the
+    handle's cached plan (no new validation, tile lists or tensor maps) and
+    gives exactly what a handle building the plan from scratch gives; a changed
+    descriptor (here the learning rate) builds a new plan."""
+    Ws, Gs, Ms, lrs = _inputs("ragged_h384", steady=True)
+    dev = torch.device("cuda", 0)
+    Wa, Ma = [w.to(dev) for w in Ws], [m.to(dev) for m in Ms]
+    Gd = [g.to(dev) for g in Gs]
+    cached = B.MuonStep(0)
+    descs, n = cached.descs_from_tensors(Wa, Gd, Ma, lrs)
+    for _ in range(3):
+        cached.step_descs(descs, n)
+    assert B.muon_plan_builds(cached.h) == 1
+    Wb, Mb = [w.to(dev) for w in Ws], [m.to(dev) for m in Ms]
+    for _ in range(3):
+        fresh = B.MuonStep(0)       # a new handle plans from scratch every step
+        fresh.step(Wb, Gd, Mb, lrs)
+        torch.cuda.synchronize()
+        assert B.muon_plan_builds(fresh.h) == 1
+        fresh.close()
+    torch.cuda.synchronize()
+    assert cached.check_status() == B.MUON_OK
+    for a, b in zip(Wa, Wb):
+        assert torch.equal(a, b)
+    for a, b in zip(Ma, Mb):
+        assert torch.equal(a, b)
+    descs2, n2 = cached.descs_from_tensors(Wa, Gd, Ma, [2 * x for x in lrs])
+    cached.step_descs(descs2, n2)
+    assert B.muon_plan_builds(cached.h) == 2
+    cached.step_descs(descs, n)       # the first batch is still cached
+    assert B.muon_plan_builds(cached.h) == 2
+    torch.cuda.synchronize()
+    cached.close()
