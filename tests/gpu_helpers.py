@@ -121,8 +121,6 @@ def check_w_against_oracle(W0, Wg, Og64, res, lr_eff, what=""):
              + 4 * 2.0 ** -24 * np.abs(x))             # the kernel's fp32 fma before the final rounding
     if W0.dtype == torch.bfloat16:
         half = 0.5 * (bf16_ulp(got) + bf16_ulp(want))
-        mism = got != want
-        assert mism.mean() <= 5e-2, f"{what} W differs from the oracle's at {mism.mean():.2%} of the elements"
     else:
         half = 2.0 ** -24 * (np.abs(got) + np.abs(want))
     err = np.abs(got - want)
