@@ -228,6 +228,28 @@ def link_rates(host, dev, reps: int = 3):
     return out[0], out[1]
 
 
+def copy_only_ms(Wh, Gh, Mh, Wd, Gd, Md, dev, reps: int = 2):
+    """Wall time (best of `reps`) of one step's copies alone: W, G, M host to
+    device on one stream while W, M go device to host on another, the same
+    pinned buffers and bytes as an end-to-end step, no kernels.  Overwrites the
+    device tensors and the host W, M."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s_in):
+            for h, d in zip(Wh + Gh + Mh, Wd + Gd + Md):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for h, d in zip(Wh + Mh, Wd + Md):
+                h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        best = min(best, (time.perf_counter() - t0) * 1e3)
+    return best
+
+
 def numa_placement(ptr: int):
     """NUMA nodes holding the pages of the mapping that contains `ptr`
     (/proc/self/numa_maps), e.g. "N0=16384", or None."""
@@ -453,6 +475,7 @@ def run_gb300(args):
         if off.check_status() != B.MUON_OK:
             raise RuntimeError("kernel status not OK after the end-to-end steps")
         off.close()
+        copy_ms = copy_only_ms(Wh, Gh, Mh, Ws, Gs, Ms, dev)
         if world > 1:
             import torch.distributed as dist
             t = torch.tensor([dt], device=dev)
@@ -466,6 +489,7 @@ def run_gb300(args):
                "pipeline": f"chunks of {args.e2e_chunk} matrices, {args.e2e_slots} device slots",
                "link_h2d_gbs": h2d_gbs, "link_d2h_gbs": d2h_gbs, "link_bound_ms_per_step": link_ms,
                "frac_of_link_bound": link_ms / (dt * 1e3),
+               "copy_only_ms_per_step": copy_ms, "frac_of_copy_only": copy_ms / (dt * 1e3),
                "host_pages_numa": numa_placement(Gh[0].data_ptr()), "gpu_numa_node": gpu_numa_node(local),
                "host_cpus": len(os.sched_getaffinity(0))}
 
