@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step in a CUDA graph and time its replays (no per-phase profile)")
+    ap.add_argument("--no-phase-profile", action="store_true",
+                    help="time the steps without the library's per-phase events, so that the handle "
+                         "replays each step as a graph (launch-bound workloads); no phases or roofline")
     return ap.parse_args()
 
 
@@ -386,10 +389,11 @@ def run_gb300(args):
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize(dev)
-    else:
+    elif not args.no_phase_profile:
         B.muon_set_profiling(ms.h, True)
         B.muon_read_profile(ms.h)  # clear
     n_launch0 = B.muon_launch_count(ms.h)
+    n_graph0 = B.muon_graph_launches(ms.h)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -409,6 +413,7 @@ def run_gb300(args):
     clk.mark(t_begin, t_end)
     clk.stop()
     launches = B.muon_launch_count(ms.h) - n_launch0 if graph is None else launches_per_step * args.steps
+    replays = B.muon_graph_launches(ms.h) - n_graph0 if graph is None else args.steps
     ms_total = e0.elapsed_time(e1)
     st, prof = B.muon_read_profile(ms.h)
     B.muon_set_profiling(ms.h, False)
@@ -524,6 +529,7 @@ def run_gb300(args):
         "phases": phase,
         "e2e": e2e,
         "gpu_launches": launches,
+        "graph_replays": replays,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

@@ -172,6 +172,13 @@ int64_t muon_launch_count(muon_handle h);
  * plan and does not add to it. */
 int64_t muon_plan_builds(muon_handle h);
 
+/* Number of steps this handle has run as a CUDA-graph replay.  A cached
+ * plan's first step launches its kernels one by one; from its second step on
+ * the handle replays them as a graph it captured once (one launch call instead
+ * of about 17), unless profiling is enabled or the caller's stream is being
+ * captured, when the kernels are launched one by one. */
+int64_t muon_graph_launches(muon_handle h);
+
 /* ---- Steps on buffers in host memory ------------------------------------
  *
  * The optimizer state may live in host memory when HBM is short: the pages

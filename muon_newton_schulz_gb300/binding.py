@@ -113,6 +113,8 @@ def load_library(build_if_missing: bool = False):
     lib.muon_launch_count.restype = c_int64
     lib.muon_plan_builds.argtypes = [H]
     lib.muon_plan_builds.restype = c_int64
+    lib.muon_graph_launches.argtypes = [H]
+    lib.muon_graph_launches.restype = c_int64
     lib.muon_host_workspace_size.argtypes = [H, POINTER(muon_matrix_desc), c_int, POINTER(muon_host_pipeline),
                                              POINTER(c_size_t)]
     lib.muon_host_workspace_size.restype = c_int
@@ -210,6 +212,10 @@ def muon_step_host(h, descs, n: int, pl: muon_host_pipeline, ws: int, ws_bytes: 
 
 def muon_plan_builds(h) -> int:
     return int(load_library().muon_plan_builds(h))
+
+
+def muon_graph_launches(h) -> int:
+    return int(load_library().muon_graph_launches(h))
 
 
 def make_descs(items):

@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstdio>
 
 #include "muon_internal.h"
@@ -1089,12 +1090,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kGram, true>::kT
   ns_tc_body<kGram, true>(p);
 }
 
+// Per device and kernel: the shared-memory opt-in is set, and the number of
+// co-resident clusters found, on the first launch only (neither changes).
+constexpr int kMaxDevices = 64;
+
+template <typename K>
+struct LaunchSetup {
+  std::atomic<int> clusters[kMaxDevices];   // 0: not yet set up
+};
+
+// Sets the dynamic shared-memory size of `kernel` on the current device once;
+// with `cluster` > 0 also returns how many clusters of that size fit at once.
+template <typename K>
+int setup_kernel(K kernel, LaunchSetup<K>& st, int smem, int threads, int sm_count, int cluster, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int v = st.clusters[dev].load(std::memory_order_acquire);
+    if (v > 0) {
+      *out = v;
+      return 0;
+    }
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return (int)e;
+  int n = 1;
+  if (cluster > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sm_count, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return (int)e;
+    if (n <= 0) return (int)cudaErrorLaunchOutOfResources;
+  }
+  if (dev >= 0 && dev < kMaxDevices) st.clusters[dev].store(n, std::memory_order_release);
+  *out = n;
+  return 0;
+}
+
 template <bool kGram>
 int launch_tc(const PhaseParams& p, int grid, void* stream, bool pdl) {
   using C = Cfg<kGram, false>;
   if (p.total_tiles == 0) return 0;
-  cudaError_t e = cudaFuncSetAttribute(k_ns_tc<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return (int)e;
+  static LaunchSetup<decltype(&k_ns_tc<kGram>)> setup;
+  int unused = 0;
+  const int e = setup_kernel(&k_ns_tc<kGram>, setup, C::kSmemBytes, C::kThreads, grid, 0, &unused);
+  if (e != 0) return e;
   if (grid > p.total_tiles) grid = p.total_tiles;
   return launch_kernel(k_ns_tc<kGram>, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, stream, pdl, p);
 }
@@ -1105,18 +1148,10 @@ template <bool kGram>
 int launch_tc_pair(const PhaseParams& p, int sm_count, void* stream, bool pdl) {
   using C = Cfg<kGram, true>;
   if (p.total_tiles == 0) return 0;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_ns_tc_pair<kGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return (int)e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)sm_count, 1, 1);
-  cfg.blockDim = dim3(C::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = (cudaStream_t)stream;
+  static LaunchSetup<decltype(&k_ns_tc_pair<kGram>)> setup;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, k_ns_tc_pair<kGram>, &cfg);
-  if (e != cudaSuccess) return (int)e;
-  if (clusters <= 0) return (int)cudaErrorLaunchOutOfResources;
+  const int e = setup_kernel(&k_ns_tc_pair<kGram>, setup, C::kSmemBytes, C::kThreads, sm_count, 2, &clusters);
+  if (e != 0) return e;
   if (clusters > sm_count / 2) clusters = sm_count / 2;
   if (clusters > p.total_tiles) clusters = p.total_tiles;
 #ifdef MUON_TC_PROFILE

@@ -58,6 +58,13 @@ struct StepPlan {
   std::vector<LaunchRec> seq;
   int iters = 0;
   int apply_launches = 0;
+  int kernels = 0;                  // kernel launches in seq
+  int uses = 0;                     // steps run from this plan
+  cudaGraphExec_t exec = nullptr;   // the launch sequence as a graph, from the second use on
+  bool graph_tried = false;
+  ~StepPlan() {
+    if (exec) cudaGraphExecDestroy(exec);
+  }
 };
 
 constexpr size_t kPlanCacheEntries = 32;
@@ -80,6 +87,9 @@ struct muon_handle_s {
   // most recently used step plans first
   std::vector<std::unique_ptr<StepPlan>> plans;
   int64_t plan_builds = 0;
+  // stream on which plans are captured into graphs, created on first use
+  cudaStream_t capture_stream = nullptr;
+  int64_t graph_launches = 0;
   // muon_step_host: copy-in, step and copy-out streams and their events,
   // created on first use
   cudaStream_t host_streams[3] = {nullptr, nullptr, nullptr};
@@ -385,7 +395,7 @@ cudaEvent_t take_event(muon_handle h) {
 
 // Cached plan for exactly these descriptors and this workspace, moved to the
 // front of the cache, or null.
-const StepPlan* find_plan(muon_handle h, const muon_matrix_desc* descs, int n, const void* ws) {
+StepPlan* find_plan(muon_handle h, const muon_matrix_desc* descs, int n, const void* ws) {
   if (n <= 0 || !descs) return nullptr;
   for (size_t i = 0; i < h->plans.size(); ++i) {
     const StepPlan& p = *h->plans[i];
@@ -489,7 +499,10 @@ muon_status make_plan(muon_handle h, const Plan& P, const muon_matrix_desc* desc
   bool pdl = false;
   auto push = [&](LaunchRec::Kind k, uint32_t idx) {
     out.seq.push_back({k, idx, pdl});
-    if (k != LaunchRec::kMark) pdl = muon::kUsePdl;
+    if (k != LaunchRec::kMark) {
+      pdl = muon::kUsePdl;
+      out.kernels += 1;
+    }
   };
   push(LaunchRec::kMark, 0);
   for (size_t b = 0; b < P.mats.size(); b += muon::kMaxEltMats) {
@@ -711,7 +724,69 @@ muon_status issue_plan(muon_handle h, const StepPlan& plan, void* stream) {
   return st;
 }
 
-// ---- steps on host-resident buffers
+// Captures a plan's launches into a graph on the handle's capture stream
+// (on failure the plan keeps running eagerly).
+void build_graph(muon_handle h, StepPlan& plan) {
+  plan.graph_tried = true;
+  if (!h->capture_stream && cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  if (cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  const int64_t launches = h->launches;
+  const std::string err = h->err;
+  const muon_status st = issue_plan(h, plan, h->capture_stream);
+  h->launches = launches;   // captured, not run
+  h->err = err;
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(h->capture_stream, &g);
+  if (st != MUON_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return;
+  }
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  plan.exec = ex;
+}
+
+// Runs one step from a plan: its first use launches the kernels one by one
+// (which also does the kernels' one-time set-up), later uses replay the plan
+// as a CUDA graph, unless profiling is on (events go between the launches) or
+// the caller's stream is being captured (the launches then join the caller's
+// graph).
+muon_status run_plan(muon_handle h, StepPlan& plan, void* stream) {
+  const int use = plan.uses++;
+  if (use > 0 && !h->profiling) {
+    DeviceGuard guard(h->device);
+    cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cst) != cudaSuccess) {
+      cudaGetLastError();
+      cst = cudaStreamCaptureStatusActive;
+    }
+    if (cst == cudaStreamCaptureStatusNone) {
+      if (!plan.exec && !plan.graph_tried) build_graph(h, plan);
+      if (plan.exec) {
+        const cudaError_t e = cudaGraphLaunch(plan.exec, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(h, MUON_ERR_CUDA, std::string("cudaGraphLaunch: ") + cudaGetErrorString(e));
+        h->launches += plan.kernels;
+        h->graph_launches += 1;
+        return MUON_OK;
+      }
+    }
+  }
+  return issue_plan(h, plan, stream);
+}
+
+// ---- steps on host-resident buffers// ---- steps on host-resident buffers
 
 constexpr uint32_t kHostBits = MUON_HOST_W | MUON_HOST_G | MUON_HOST_M | MUON_HOST_O;
 
@@ -875,6 +950,8 @@ muon_status muon_destroy(muon_handle h) {
     for (cudaEvent_t e : h->host_events) cudaEventDestroy(e);
     for (cudaStream_t st : h->host_streams)
       if (st) cudaStreamDestroy(st);
+    h->plans.clear();   // their graphs, with this device current
+    if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   }
   delete h;
   return MUON_OK;
@@ -973,11 +1050,11 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   h->err.clear();
   // a batch seen before (same descriptor bytes, same workspace) reuses its
   // validated plan, parameter blocks and tensor maps
-  const StepPlan* plan = find_plan(h, descs, n, ws);
+  StepPlan* plan = find_plan(h, descs, n, ws);
   if (plan) {
     if (ws_bytes < plan->need)
       return fail(h, MUON_ERR_WORKSPACE, "workspace too small: need " + std::to_string(plan->need) + " bytes");
-    return issue_plan(h, *plan, stream);
+    return run_plan(h, *plan, stream);
   }
   std::string why;
   std::vector<Range> ranges;
@@ -1003,10 +1080,12 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n, void*
   h->plan_builds += 1;
   if (h->plans.size() >= kPlanCacheEntries) h->plans.pop_back();
   h->plans.insert(h->plans.begin(), std::move(fresh));
-  return issue_plan(h, *h->plans.front(), stream);
+  return run_plan(h, *h->plans.front(), stream);
 }
 
 int64_t muon_plan_builds(muon_handle h) { return h ? h->plan_builds : 0; }
+
+int64_t muon_graph_launches(muon_handle h) { return h ? h->graph_launches : 0; }
 
 muon_status muon_host_workspace_size(muon_handle h, const muon_matrix_desc* descs, int n,
                                      const muon_host_pipeline* pl, size_t* bytes) {

@@ -261,6 +261,7 @@ def test_repeated_batch_reuses_its_plan():
     for _ in range(3):
         cached.step_descs(descs, n)
     assert B.muon_plan_builds(cached.h) == 1
+    assert B.muon_graph_launches(cached.h) == 2   # the first step of a plan runs eagerly
     Wb, Mb = [w.to(dev) for w in Ws], [m.to(dev) for m in Ms]
     for _ in range(3):
         fresh = B.MuonStep(0)       # a new handle plans from scratch every step
@@ -281,3 +282,43 @@ def test_repeated_batch_reuses_its_plan():
     assert B.muon_plan_builds(cached.h) == 2
     torch.cuda.synchronize()
     cached.close()
+
+
+def test_cached_plan_replays_as_a_graph():
+    """From a cached plan's second step on, the handle replays the step as a
+    CUDA graph it captured once; replays equal eager steps bit for bit, on any
+    stream, and profiling switches back to launching the kernels one by one."""
+    Ws, Gs, Ms, lrs = _inputs("ragged_h384", steady=True)
+    dev = torch.device("cuda", 0)
+    Gd = [g.to(dev) for g in Gs]
+    Wa, Ma = [w.to(dev) for w in Ws], [m.to(dev) for m in Ms]   # replayed
+    Wb, Mb = [w.to(dev) for w in Ws], [m.to(dev) for m in Ms]   # eager (profiling on)
+    rep = B.MuonStep(0)
+    eager = B.MuonStep(0)
+    assert B.muon_set_profiling(eager.h, True) == B.MUON_OK
+    d_rep, n = rep.descs_from_tensors(Wa, Gd, Ma, lrs)
+    d_eag, _ = eager.descs_from_tensors(Wb, Gd, Mb, lrs)
+    side = torch.cuda.Stream(dev)
+    per_step = None
+    for k in range(4):
+        before = B.muon_launch_count(rep.h)
+        if k == 2:
+            with torch.cuda.stream(side):
+                rep.step_descs(d_rep, n, stream=side.cuda_stream)
+            torch.cuda.current_stream(dev).wait_stream(side)
+        else:
+            rep.step_descs(d_rep, n)
+        eager.step_descs(d_eag, n)
+        per_step = per_step or B.muon_launch_count(rep.h) - before
+        assert B.muon_launch_count(rep.h) - before == per_step
+    torch.cuda.synchronize()
+    assert B.muon_graph_launches(rep.h) == 3 and B.muon_graph_launches(eager.h) == 0
+    assert rep.check_status() == B.MUON_OK and eager.check_status() == B.MUON_OK
+    for a, b in zip(Wa, Wb):
+        assert torch.equal(a, b)
+    for a, b in zip(Ma, Mb):
+        assert torch.equal(a, b)
+    st, prof = B.muon_read_profile(eager.h)
+    assert st == B.MUON_OK and prof.steps == 4
+    rep.close()
+    eager.close()
