@@ -67,3 +67,23 @@ def test_host_step_time_out_is_reported(monkeypatch):
         assert torch.equal(a, b)      # no chunk applied an update
     assert off.check_status() == B.MUON_OK
     off.close()
+
+
+def test_host_step_with_every_buffer_on_the_device_is_muon_step():
+    """host_buffers = 0: nothing is staged or copied; each chunk's step runs on
+    the caller's device buffers in place and equals one muon_step."""
+    Ws, Gs, Ms, lrs = wl.make_workload(wl.WORKLOADS["odd_shapes"], "cpu", steady_momentum=True)
+    dev = torch.device("cuda", 0)
+    Wa, Ga, Ma = [w.to(dev) for w in Ws], [g.to(dev) for g in Gs], [m.to(dev) for m in Ms]
+    Wb, Mb = [w.to(dev) for w in Ws], [m.to(dev) for m in Ms]
+    ms = B.MuonStep(0)
+    ms.step(Wa, Ga, Ma, lrs)
+    off = HostOffloadedMuon(0, chunk=2, slots=2, host_buffers=0)
+    off.step(Wb, Ga, Mb, lrs)
+    assert off.check_status() == B.MUON_OK
+    for a, b in zip(Wa, Wb):
+        assert torch.equal(a, b)
+    for a, b in zip(Ma, Mb):
+        assert torch.equal(a, b)
+    off.close()
+    ms.close()
