@@ -145,8 +145,10 @@ muon_status muon_step(muon_handle h, const muon_matrix_desc* descs, int n,
  * `ws`: MUON_ERR_TIMEOUT if a kernel of an earlier step gave up a bounded
  * wait, else MUON_OK (or MUON_ERR_CUDA if the stream reports an error).
  * ws == NULL reads and clears the status word of muon_step_noalloc's fixed
- * array on the handle's device.  A step whose wait timed out leaves W
- * unchanged when the time-out happened before its last kernel started. */
+ * array on the handle's device; the workspace of the handle's most recent
+ * muon_step_host call holds one status word per staging slot, and all of them
+ * are read and cleared.  A step whose wait timed out leaves W unchanged when
+ * the time-out happened before its last kernel started. */
 muon_status muon_check_status(muon_handle h, void* ws, void* stream);
 
 muon_status muon_destroy(muon_handle h);
@@ -217,7 +219,11 @@ muon_status muon_host_workspace_size(muon_handle h, const muon_matrix_desc* desc
  * and untouched until `stream` has passed the step: the call only enqueues
  * work.  The handle's copy and step streams wait for the work already on
  * `stream`, and `stream` waits for their last copy.  Errors as muon_step; a
- * descriptor error launches and copies nothing. */
+ * descriptor error launches and copies nothing; a launch error part-way
+ * returns MUON_ERR_CUDA with copies of earlier chunks possibly still in flight
+ * on the handle's streams (synchronise the device before reusing the host
+ * buffers).  muon_check_status(h, ws, stream) reads the status words of every
+ * chunk's step. */
 muon_status muon_step_host(muon_handle h, const muon_matrix_desc* descs, int n,
                            const muon_host_pipeline* pl, void* ws, size_t ws_bytes, void* stream);
 
