@@ -68,3 +68,25 @@ def test_dampened_momentum(mode, nesterov):
     momentum state: M within one fp32 ulp of the oracle, O within tolerance."""
     tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
     run_and_check("ragged_h384", mode=mode, tol_o=tol, nesterov=nesterov, dampening=True, steady_momentum=True)
+
+
+@pytest.mark.parametrize("mode", [B.MUON_MODE_BF16, B.MUON_MODE_FP32_VALIDATE])
+def test_extreme_aspect_ratios(mode):
+    """Very long contractions and degenerate sizes: Gram X X^T with K = 100000
+    (1563 k-blocks, the last one half outside the matrix), a tall 100000 x 48
+    matrix (transposed in the momentum kernel and back through the W tensor
+    map), one row of 300000, and a 4 x 4 matrix; all against the oracle."""
+    import torch
+    from muon_newton_schulz_gb300 import workloads as wl
+    from gpu_helpers import check_matrix, oracle_for, run_gpu
+    tol = 2e-2 if mode == B.MUON_MODE_BF16 else 1e-4
+    specs = [(64, 100000, "bf16"), (100000, 48, "f32"), (1, 300000, "bf16"), (4, 4, "f32")]
+    Ws, Gs, Ms, lrs = [], [], [], []
+    for k, (r, c, wdt) in enumerate(specs):
+        spec = wl.MatrixSpec(r, c, 1, "gauss", 1e-3, w_dtype=wdt)
+        W, G, M = wl.make_matrix(spec, 91000 + k, "cpu", steady_momentum=True)
+        Ws.append(W); Gs.append(G); Ms.append(M); lrs.append(2e-4)
+    Wg, Mg, Og = run_gpu(Ws, Gs, Ms, lrs, mode=mode)
+    for i in range(len(Ws)):
+        res = oracle_for(Ws[i], Gs[i], Ms[i], lrs[i])
+        check_matrix(Ws[i], Gs[i], Ms[i], lrs[i], Wg[i], Mg[i], Og[i], res, tol, f"{tuple(Ws[i].shape)}")
