@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <array>
@@ -682,21 +683,29 @@ muon_status issue_plan(muon_handle h, const StepPlan& plan, void* stream) {
         }
         continue;
       case LaunchRec::kMomentum:
+        nvtxRangePushA("muon.momentum_norm");
         rc = muon::launch_momentum_norm(plan.elt[r.index], stream, r.pdl);
+        nvtxRangePop();
         what = "momentum/norm kernel";
         break;
       case LaunchRec::kFinalize:
+        nvtxRangePushA("muon.norm_finalize");
         rc = muon::launch_norm_finalize(plan.elt[r.index], stream, r.pdl);
+        nvtxRangePop();
         what = "norm finalize kernel";
         break;
       case LaunchRec::kApply:
+        nvtxRangePushA("muon.apply");
         rc = muon::launch_apply(plan.elt[r.index], stream, r.pdl);
+        nvtxRangePop();
         what = "apply kernel";
         break;
       case LaunchRec::kGram:
       case LaunchRec::kGemm: {
         const bool gram = r.kind == LaunchRec::kGram;
         const PhaseParams& pp = plan.phase[r.index];
+        // one range per launch: the phase's name as the bench's profile uses it
+        nvtxRangePushA(!gram ? "muon.gemm_update" : (pp.ngroups > 0 && pp.g[0].prev ? "muon.gram_aa_combine" : "muon.gram_xxt"));
         if (h->cfg.mode == MUON_MODE_BF16 && muon::kUsePair)
           rc = gram ? muon::launch_gram_tc_pair(pp, h->sm_count, stream, r.pdl)
                     : muon::launch_gemm_tc_pair(pp, h->sm_count, stream, r.pdl);
@@ -705,6 +714,7 @@ muon_status issue_plan(muon_handle h, const StepPlan& plan, void* stream) {
                     : muon::launch_gemm_tc(pp, h->sm_count, stream, r.pdl);
         else
           rc = gram ? muon::launch_gram_f32(pp, stream, r.pdl) : muon::launch_gemm_f32(pp, stream, r.pdl);
+        nvtxRangePop();
         what = gram ? "Gram kernel" : "GEMM kernel";
         break;
       }
@@ -775,7 +785,9 @@ muon_status run_plan(muon_handle h, StepPlan& plan, void* stream) {
     if (cst == cudaStreamCaptureStatusNone) {
       if (!plan.exec && !plan.graph_tried) build_graph(h, plan);
       if (plan.exec) {
+        nvtxRangePushA("muon.step_graph_replay");
         const cudaError_t e = cudaGraphLaunch(plan.exec, reinterpret_cast<cudaStream_t>(stream));
+        nvtxRangePop();
         if (e != cudaSuccess) return fail(h, MUON_ERR_CUDA, std::string("cudaGraphLaunch: ") + cudaGetErrorString(e));
         h->launches += plan.kernels;
         h->graph_launches += 1;
