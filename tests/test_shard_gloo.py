@@ -1,6 +1,7 @@
 """Whole-matrix ownership across ranks (CPU, gloo, world size 2): every
 matrix is stepped exactly once, by its owner, with no data exchange; the
 gathered results equal a single-process run; the split is balanced."""
+import io
 import os
 import socket
 
@@ -136,7 +137,11 @@ def _flex_worker(rank, world, port, out, steps):
             # a new gradient each step, the same on every rank (shards of it)
             G_step = {i: (local[i][1] * (1.0 + s)) for i in local}
             runner.step({i: (local[i][0], G_step[i], local[i][2]) for i in local}, lrs)
-        out.put((rank, {i: (local[i][0], local[i][2]) for i in local}, calls))
+        # by value: tensors sent through the queue would live in this
+        # process's shared memory, which is gone once it exits
+        buf = io.BytesIO()
+        torch.save({i: (local[i][0], local[i][2]) for i in local}, buf)
+        out.put((rank, buf.getvalue(), calls))
     finally:
         dist.destroy_process_group()
 
@@ -152,7 +157,7 @@ def test_flexshard_two_ranks_equal_single_process():
     procs = [ctx.Process(target=_flex_worker, args=(r, world, port, out, steps)) for r in range(world)]
     for p in procs:
         p.start()
-    got = dict((r, (loc, calls)) for r, loc, calls in (out.get(timeout=180) for _ in range(world)))
+    got = dict((r, (torch.load(io.BytesIO(loc)), calls)) for r, loc, calls in (out.get(timeout=180) for _ in range(world)))
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
