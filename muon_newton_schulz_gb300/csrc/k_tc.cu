@@ -150,7 +150,9 @@ struct Tile { int g, mat, bi, bj; };
 // last launch of a kind wins):
 //   [0] MMA issuer: accumulator granted     [1] MMA issuer: last MMA of the tile issued
 //   [2] epilogue warp 0: accumulator full   [3] epilogue warp 0: tile done
-// g_tc_life: CTA set-up done and CTA end.
+// g_tc_life: %globaltimer (ns) at [0] kernel entry, [1] after the grid
+// dependency wait (set-up done, the previous kernel complete), [2] CTA end;
+// [3..5] clock64 at the same points.
 // g_tc_epi: cycles the tracing epilogue warp (lane 0 of warp quarter 0 of the
 // leader) spends in [0] X-prefetch waits, [1] waits for its previous TMA
 // store to release the staging buffer, [2] TMEM load waits (GEMM).
@@ -160,7 +162,7 @@ struct Tile { int g, mat, bi, bj; };
 #ifdef MUON_TC_TRACE
 constexpr int kTraceCtas = 160, kTraceTiles = 96;
 __device__ long long g_tc_trace[4][kTraceCtas][kTraceTiles][4];
-__device__ long long g_tc_life[4][kTraceCtas][2];
+__device__ long long g_tc_life[4][kTraceCtas][6];
 __device__ long long g_tc_epi[4][kTraceCtas][4];
 __device__ long long g_tc_mma[4][kTraceCtas][4];
 #define TC_KIND (kGram ? (p.g[0].prev ? 1 : 0) : (p.apply ? 3 : 2))
@@ -170,7 +172,10 @@ __device__ long long g_tc_mma[4][kTraceCtas][4];
   } while (0)
 #define TC_LIFE(slot)                                                              \
   do {                                                                             \
-    if (blockIdx.x < kTraceCtas) g_tc_life[TC_KIND][blockIdx.x][(slot)] = clock64(); \
+    if (blockIdx.x < kTraceCtas) {                                                 \
+      g_tc_life[TC_KIND][blockIdx.x][(slot)] = (long long)ptx::globaltimer();      \
+      g_tc_life[TC_KIND][blockIdx.x][(slot) + 3] = clock64();                      \
+    }                                                                              \
   } while (0)
 #define TC_EPI_T0(v) const long long v = clock64()
 #define TC_EPI_ADD(ec, kind, slot, v)                                                               \
@@ -495,51 +500,40 @@ __device__ __forceinline__ void gram_values(const PhaseParams& p, const PhaseGro
   }
 }
 
-// Diagonal 32 x 32 block of a Gram tile: masked direct stores of r <= c and
-// the mirror of r < c; the diagonal value itself (or its bf16 residual) goes
-// to diag_out.
-__device__ __forceinline__ void gram_store_diag_block(const PhaseParams& p, const PhaseGroup& G, const Tile& tl,
-                                                      int row, int c0, float (&f)[32]) {
-  const int m = G.m;
-  if (row >= m) return;
-  if (G.diag_out) {
-    float* dout = G.diag_out + (int64_t)tl.mat * G.diag_stride;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (c0 + j == row) {
-        const float d = f[j];
-        if (p.diag_exact) {
-          dout[row] = d;
-          f[j] = 0.f;
-        } else {
-          dout[row] = d - __bfloat162float(__float2bfloat16_rn(d));
-        }
-      }
-    }
-  }
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(G.out) + (int64_t)tl.mat * G.out_stride;
-  const int64_t ld = G.ld_out;
+// The diagonal value of a diagonal 32 x 32 block (or its bf16 residual) goes
+// to diag_out; with diag_exact the block keeps a zero in its place.
+__device__ __forceinline__ void gram_diag_out(const PhaseParams& p, const PhaseGroup& G, const Tile& tl, int row,
+                                              int c0, float (&f)[32]) {
+  if (!G.diag_out || row >= G.m) return;
+  float* dout = G.diag_out + (int64_t)tl.mat * G.diag_stride;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const int c = c0 + j;
-    if (c < m && row <= c) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(f[j]);
-      out[(int64_t)row * ld + c] = h;
-      if (row < c) out[(int64_t)c * ld + row] = h;
+    if (c0 + j == row) {
+      const float d = f[j];
+      if (p.diag_exact) {
+        dout[row] = d;
+        f[j] = 0.f;
+      } else {
+        dout[row] = d - __bfloat162float(__float2bfloat16_rn(d));
+      }
     }
   }
 }
 
-// Chunk wholly above the diagonal: stage the 32 x 32 block and its transpose
-// in shared memory and write both with TMA stores.  Staging per warp (8 KiB):
-// Gram 1 double-buffers the (block, transpose) pair at 0 / 2048 and
+// Store one 32 x 32 block of a Gram tile on or above the diagonal with TMA
+// (rows and columns past m are clipped by the tensor map).  Staging per warp
+// (8 KiB): Gram 1 double-buffers a (block, transpose) pair at 0 / 2048 and
 // 4096 / 6144; Gram 2 has one pair at 0 / 2048 and its prefetched blocks of
 // the previous A at 4096 and 6144.
-__device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, const Tile& tl, EpiCtx& ec, int r0,
-                                                       int c0, const float (&f)[32], bool single) {
+//   Above the diagonal: the block and its transpose, two stores.
+//   On the diagonal (c0 == r0): each row is written whole, then its part below
+//   the diagonal is overwritten with the mirror of the part above, so the
+//   stored block is exactly symmetric; one store.
+__device__ __forceinline__ void gram_store_block(const PhaseParams& p, const Tile& tl, EpiCtx& ec, int r0, int c0,
+                                                 const float (&f)[32], bool single, bool diag) {
   const int o = single ? 0 : ec.obuf;
   uint8_t* ro = ec.buf + o * 4096;
-  uint8_t* tr = ro + 2048;
+  uint8_t* tr = diag ? ro : ro + 2048;
   const int lane = ec.lane;
   if (lane == 0) {   // the stores that last read this buffer are done with it
     TC_EPI_T0(t_w);
@@ -557,16 +551,19 @@ __device__ __forceinline__ void gram_store_upper_block(const PhaseParams& p, con
     u.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
     *reinterpret_cast<uint4*>(ro + ptx::sw64_off(lane, i)) = u;
   }
-  // transposed block: row j (= column c0 + j), column lane (= row r0 + lane)
+  if (diag) __syncwarp();   // the mirror below overwrites other lanes' rows
+  // transposed block: row j (= column c0 + j), column lane (= row r0 + lane);
+  // on the diagonal only its part below the diagonal (j > lane)
 #pragma unroll
   for (int j = 0; j < 32; ++j)
-    *reinterpret_cast<__nv_bfloat16*>(tr + ptx::sw64_off(j, lane >> 3) + (lane & 7) * 2) = __float2bfloat16_rn(f[j]);
+    if (!diag || j > lane)
+      *reinterpret_cast<__nv_bfloat16*>(tr + ptx::sw64_off(j, lane >> 3) + (lane & 7) * 2) = __float2bfloat16_rn(f[j]);
   ptx::fence_async_smem();
   __syncwarp();
   if (lane == 0) {
     const CUtensorMap* mc = &p.map_c[tl.g];
     ptx::tma_store_4d(mc, ro, c0, r0, tl.mat, 0);
-    ptx::tma_store_4d(mc, tr, r0, c0, tl.mat, 0);
+    if (!diag) ptx::tma_store_4d(mc, tr, r0, c0, tl.mat, 0);
     ptx::bulk_commit();
   }
   if (!single) ec.obuf ^= 1;
@@ -619,8 +616,9 @@ __device__ __forceinline__ bool gram_chunk(const PhaseParams& p, const PhaseGrou
   }
   float f[32];
   gram_values(p, G, tl, row, c0, col0, v, pa, gd, f);
-  if (c0 == r0) gram_store_diag_block(p, G, tl, row, c0, f);
-  else gram_store_upper_block(p, tl, ec, r0, c0, f, G.prev != nullptr);
+  const bool diag = c0 == r0;
+  if (diag) gram_diag_out(p, G, tl, row, c0, f);
+  gram_store_block(p, tl, ec, r0, c0, f, G.prev != nullptr, diag);
   return true;
 }
 
@@ -999,6 +997,7 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
     pi.nunits = gridDim.x;
   }
   TC_PROF_T0(t_cta);
+  if (threadIdx.x == 0) TC_LIFE(0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -1038,7 +1037,7 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
   // of the step produced
   grid_dependency_wait();
   if (threadIdx.x == 0) allow_dependent_launch();
-  if (threadIdx.x == 0) TC_LIFE(0);
+  if (threadIdx.x == 0) TC_LIFE(1);
 
   if (warp == 0) {
     if (lane == 0) run_producer<kGram, kPair>(p, pi, smem, full, empty, abort);
@@ -1076,7 +1075,7 @@ __device__ __forceinline__ void ns_tc_body(const PhaseParams& p) {
 #ifdef MUON_TC_PROFILE
   if (threadIdx.x == 0) TC_PROF_ADD(5, t_cta);
 #endif
-  if (threadIdx.x == 0) TC_LIFE(1);
+  if (threadIdx.x == 0) TC_LIFE(2);
 }
 
 template <bool kGram>

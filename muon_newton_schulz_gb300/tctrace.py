@@ -16,7 +16,16 @@ update): medians over the leader CTAs of the pairs of
 - ``mma_exec``: ``issue - mma_wait_stages``, to compare with the ideal
   (128 cycles per 256 x 256 x 16 CTA-pair MMA);
 - ``epi``: the epilogue warp's time from "accumulator full" to "tile done",
-  and its waits for prefetched inputs and for staging buffers.
+  and its waits for prefetched inputs and for staging buffers;
+- ``launch_us``: from the first CTA's entry to the last CTA's end
+  (%globaltimer, all CTAs), with ``entry_spread_us`` (last entry - first),
+  ``setup_us`` (median entry to the end of the grid dependency wait: set-up
+  and the wait for the previous kernel), ``work_us`` (median from there to
+  the CTA's end) and ``end_spread_us`` (last end - first end);
+  ``sm_mhz``: the median CTA's clock64 cycles over its globaltimer time
+  from entry to end; ``fill_cycles``: median from the end of the grid
+  dependency wait to the first tile's accumulator grant; ``drain_cycles``:
+  median from the last tile done to the CTA's end (leader CTAs).
 
 The stamps of the last launch of each kind are kept; the epilogue wait
 counters are summed over the traced step's launches of that kind and divided
@@ -30,7 +39,7 @@ import json
 import os
 
 KINDS = ("gram_xxt", "gram_aa_combine", "gemm", "gemm_apply")
-# the kernel's trace arrays: [kind][cta][tile][4] stamps, [kind][cta][2] life,
+# the kernel's trace arrays: [kind][cta][tile][4] stamps, [kind][cta][6] life,
 # [kind][cta][4] epilogue waits, [kind][cta][4] MMA waits
 K_KINDS, K_CTAS, K_TILES = 4, 160, 96
 
@@ -61,7 +70,7 @@ def main():
     read.restype = ctypes.c_int
     n_tr = K_KINDS * K_CTAS * K_TILES * 4
     n_small = K_KINDS * K_CTAS
-    buf = np.zeros(n_tr + n_small * (2 + 4 + 4), dtype=np.int64)
+    buf = np.zeros(n_tr + n_small * (6 + 4 + 4), dtype=np.int64)
 
     dev = torch.device("cuda", 0)
     w = wl.WORKLOADS[args.workload or wl.HEADLINE]
@@ -82,8 +91,8 @@ def main():
 
     tr = buf[:n_tr].reshape(K_KINDS, K_CTAS, K_TILES, 4)
     o = n_tr
-    life = buf[o:o + n_small * 2].reshape(K_KINDS, K_CTAS, 2)
-    o += n_small * 2
+    life = buf[o:o + n_small * 6].reshape(K_KINDS, K_CTAS, 6)
+    o += n_small * 6
     epi = buf[o:o + n_small * 4].reshape(K_KINDS, K_CTAS, 4)
     o += n_small * 4
     mma = buf[o:o + n_small * 4].reshape(K_KINDS, K_CTAS, 4)
@@ -98,7 +107,10 @@ def main():
                 continue
             g0, g1, e0, e1 = t[:n, 0], t[:n, 1], t[:n, 2], t[:n, 3]
             launches = max(per_kind[k], 1)
+            lc = life[k, c]
             rows.append({
+                "fill_cycles": float(g0[0] - lc[4]),
+                "drain_cycles": float(lc[5] - e1[n - 1]),
                 "tiles": n,
                 "period": float(np.median(np.diff(g0))),
                 "issue": float(np.median(g1 - g0)),
@@ -113,6 +125,18 @@ def main():
         med = {key: round(float(np.median([r[key] for r in rows])), 1) for key in rows[0]}
         med["mma_exec"] = round(med["issue"] - med["mma_wait_stages"], 1)
         med["leader_ctas"] = len(rows)
+        lf = life[k]
+        lf = lf[lf[:, 0] != 0]
+        if len(lf):
+            us = lambda v: round(float(v) / 1e3, 2)
+            med["launch_us"] = us(lf[:, 2].max() - lf[:, 0].min())
+            med["entry_spread_us"] = us(lf[:, 0].max() - lf[:, 0].min())
+            med["setup_us"] = us(np.median(lf[:, 1] - lf[:, 0]))
+            med["work_us"] = us(np.median(lf[:, 2] - lf[:, 1]))
+            med["end_spread_us"] = us(lf[:, 2].max() - lf[:, 2].min())
+            med["ctas"] = int(len(lf))
+            mhz = (lf[:, 5] - lf[:, 3]) / np.maximum(lf[:, 2] - lf[:, 0], 1) * 1e3
+            med["sm_mhz"] = round(float(np.median(mhz)), 0)
         out[name] = med
     print(json.dumps(out, indent=1))
 
