@@ -230,6 +230,14 @@ __device__ __forceinline__ Tile decode_tile(const PhaseParams& p, int t, bool gr
   return tl;
 }
 
+// A CTA pair's Gram tile on the diagonal (bi == bj): CTA r's left operand
+// (rows 256 bi + 128 r) and its half of the right operand (rows
+// 256 bj + 128 r) are the same rows of the same matrix.
+template <bool kGram, bool kPair>
+__device__ __forceinline__ bool gram_diag_tile(const Tile& tl) {
+  return kGram && kPair && tl.bi == tl.bj;
+}
+
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -269,6 +277,10 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, const PairInf
     const CUtensorMap* mb = &p.map_b[tl.g];
     const int arow = tl.bi * C::kTileM + TC * pi.rank;     // this CTA's left-operand rows
     const int bcol = tl.bj * TN + C::kBCols * pi.rank;     // this CTA's right-operand rows/columns
+    // a pair's Gram tile on the diagonal: each CTA's right-operand half is
+    // its left operand (the same rows), loaded once
+    const bool same = gram_diag_tile<kGram, kPair>(tl);
+    const uint32_t stage_bytes = same ? (uint32_t)A_BYTES : (uint32_t)C::kStageBytes;
     for (int kb = 0; kb < nk; ++kb) {
       TC_PROF_T0(t_e);
       if (!wait_role<false>(&empty[stage], phase ^ 1u, abort, p.status, kStatusTimeoutProducer)) {
@@ -285,12 +297,14 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, const PairInf
         // MMA's bounded wait runs out and the kernel reports a time-out
       } else if (!kPair || pi.rank == 0) {
         // the even CTA's barrier counts the bytes of both CTAs of a pair
-        ptx::mbar_arrive_expect_tx(&full[stage], (kPair ? 2 : 1) * C::kStageBytes);
+        ptx::mbar_arrive_expect_tx(&full[stage], (kPair ? 2u : 1u) * stage_bytes);
         if (kGram) {
           ptx::tma_load_4d(sa, ma, k0, arow, tl.mat, G.buf_in, &full[stage]);
+          if (!same) {
 #pragma unroll
-          for (int q = 0; q < C::kBCols / TC; ++q)
-            ptx::tma_load_4d(sb + q * A_BYTES, ma, k0, bcol + TC * q, tl.mat, G.buf_in, &full[stage]);
+            for (int q = 0; q < C::kBCols / TC; ++q)
+              ptx::tma_load_4d(sb + q * A_BYTES, ma, k0, bcol + TC * q, tl.mat, G.buf_in, &full[stage]);
+          }
         } else {
           ptx::tma_load_4d(sa, ma, k0, arow, tl.mat, 0, &full[stage]);
 #pragma unroll
@@ -303,7 +317,7 @@ __device__ __forceinline__ void run_producer(const PhaseParams& p, const PairInf
         const uint32_t bar = ptx::mapa(ptx::smem_u32(&full[stage]), 0);
         if (kGram) {
           ptx::tma_load_4d_pair(sa, ma, k0, arow, tl.mat, G.buf_in, bar);
-          ptx::tma_load_4d_pair(sb, ma, k0, bcol, tl.mat, G.buf_in, bar);
+          if (!same) ptx::tma_load_4d_pair(sb, ma, k0, bcol, tl.mat, G.buf_in, bar);
         } else {
           ptx::tma_load_4d_pair(sa, ma, k0, arow, tl.mat, 0, bar);
 #pragma unroll
@@ -345,6 +359,7 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
   for (int t = pi.unit; ok && t < p.total_tiles; t += pi.nunits, ++lt) {
     const Tile tl = decode_tile<kPair>(p, t, kGram);
     const int nk = (p.g[tl.g].K + TK - 1) / TK;
+    const bool same = gram_diag_tile<kGram, kPair>(tl);   // right operand = the left one
     TC_PROF_T0(t_a);
     if (!wait_role<kPair>(&tempty[acc], acc_phase ^ 1u, abort, p.status, kStatusTimeoutMma)) {
       ok = false;
@@ -373,7 +388,7 @@ __device__ __forceinline__ void run_mma(const PhaseParams& p, const PairInfo& pi
         const uint64_t ad = ptx::smem_desc(sa + kk * UK * 2, 16, 1024);
         uint64_t bd;
         if (kGram) {
-          bd = ptx::smem_desc(sb + kk * UK * 2, 16, 1024);
+          bd = ptx::smem_desc((same ? sa : sb) + kk * UK * 2, 16, 1024);
         } else {
           // MN-major, 128B swizzle: 64-element MN blocks 8 KiB apart (LBO),
           // 8-row K groups 1024 B apart (SBO); UK rows of K = 2 KiB.
