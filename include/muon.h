@@ -133,7 +133,7 @@ muon_status muon_workspace_size(muon_handle h, const muon_matrix_desc* descs, in
  * call while it runs on `stream` (its contents need not be preserved between
  * calls).  n == 0 launches nothing and returns MUON_OK.
  *
- * The handle keeps the plans of its most recent batches (up to 8): a call
+ * The handle keeps the plans of its most recent batches (up to 32): a call
  * whose descriptor array is byte-for-byte one seen before, with the same
  * workspace pointer, skips validation and planning and launches the kernels
  * with the parameter blocks and TMA tensor maps built then (they depend on
