@@ -12,7 +12,9 @@ update): medians over the leader CTAs of the pairs of
 - ``period``: cycles from one tile's accumulator grant to the next;
 - ``issue``: from the grant to the tile's last MMA issued (the MMA issuer is
   throttled by the tensor pipe, so this is the pipe's time for the tile);
-- ``mma_wait_stages``: cycles the MMA issuer waited for a full ring stage;
+- ``mma_wait_stages``: cycles the MMA issuer waited for a full ring stage
+  per tile, and of those ``mma_wait_first_kblock`` / ``mma_wait_first_4_kblocks``
+  on the tile's first one / four k-blocks;
 - ``mma_exec``: ``issue - mma_wait_stages``, to compare with the ideal
   (128 cycles per 256 x 256 x 16 CTA-pair MMA);
 - ``epi``: the epilogue warp's time from "accumulator full" to "tile done",
@@ -115,6 +117,8 @@ def main():
                 "period": float(np.median(np.diff(g0))),
                 "issue": float(np.median(g1 - g0)),
                 "mma_wait_stages": float(mma[k, c, 2]) / n,
+                "mma_wait_first_kblock": float(mma[k, c, 0]) / n,
+                "mma_wait_first_4_kblocks": float(mma[k, c, 1]) / n,
                 "mma_idle_between_tiles": float(np.median(g0[1:] - g1[:-1])),
                 "epi": float(np.median(e1 - e0)),
                 "epi_wait_inputs": float(epi[k, c, 0]) / n / launches,
